@@ -1,0 +1,192 @@
+/*
+ * attn.h -- C ABI of libattn.so: attention forward with online softmax on
+ * GB300 (sm_103a).
+ *
+ * Two forms of O = softmax(scale * Q K^T [+ causal mask]) V, both computed
+ * without ever writing S or P to global memory:
+ *
+ *   attn_fwd    multi-head prefill, FlashAttention-2 loop order ("FP32
+ *               CUDA-core FlashAttention-2 v2" blog, dandandamowang
+ *               post_1787450400: section 1.1 Q-outer/KV-inner loop, 1.2
+ *               on-chip m/l/O, 1.3 deferred 1/l, 1.4 and 3.4 causal block
+ *               skipping with diagonal-block masking, 3.5 single write of O).
+ *   mla_decode  MLA absorbed decode over a paged 576-wide latent cache ("MLA
+ *               x FlashAttention-3 fusion" article, hnwysp news 119127:
+ *               latent layout [c_kv 512 | k_rope 64], the absorption
+ *               identity Q K^T = (Q W_UK) c^T + Q_R k_R^T, and the
+ *               online-softmax "partial reduction" stage of its pipeline).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA
+ *     memory) of the current device, except where a comment says HOST.
+ *   - The caller owns every buffer.  The library allocates no device memory
+ *     per call; the kernels allocate and free tensor memory (TMEM) inside
+ *     each CTA.  Tensor-map descriptors are built on the host per call and
+ *     passed by value as kernel parameters.
+ *   - Calls are asynchronous: they validate, enqueue on `stream`
+ *     (cudaStream_t; NULL = the legacy default stream) and return.  They
+ *     never synchronise and never trap.  Errors that only the device can see
+ *     (a bad block-table entry, a wait that ran out) are recorded in a
+ *     device error word and returned later by attn_device_status().
+ *   - Return value: ATTN_OK (0) or a negative ATTN_ERR_* code; on error
+ *     nothing was launched and attn_last_error() describes the cause.
+ *   - Thread safety: calls may be made from several host threads; the error
+ *     message is thread-local.
+ */
+#ifndef GB300_ATTN_H_
+#define GB300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG (-1)      /* null pointer, size <= 0, non-finite scale */
+#define ATTN_ERR_UNSUPPORTED (-2)      /* head dim / dtype / head count not built */
+#define ATTN_ERR_MISALIGNED (-3)       /* a base pointer is not 16-byte aligned */
+#define ATTN_ERR_WORKSPACE_TOO_SMALL (-4)
+#define ATTN_ERR_CUDA (-5)             /* a CUDA runtime / driver call failed */
+#define ATTN_ERR_BAD_BLOCK_TABLE (-6)  /* device: block id outside [0, num_blocks) */
+#define ATTN_ERR_BAD_SEQLEN (-7)       /* device: seqlen < 0 or > max_blocks*64 */
+#define ATTN_ERR_DEVICE_TIMEOUT (-8)   /* device: a pipeline wait ran out (~2 s) */
+
+/* ---- data types -------------------------------------------------------- */
+#define ATTN_DTYPE_F32 0   /* fp32 in, fp32 out, fp32 arithmetic (CUDA cores) */
+#define ATTN_DTYPE_BF16 1  /* bf16 in, bf16 out, fp32 accumulate (tcgen05) */
+
+/*
+ * attn_fwd -- multi-head attention forward (prefill).
+ *
+ *   q, k, v : [B, H, N, D] contiguous, element type `dtype`.
+ *   o       : [B, H, N, D] contiguous, element type `dtype` (written).
+ *   lse     : [B, H, N] float32 (written): natural-log logsumexp of the
+ *             scaled, masked scores of each row.  The pages never output it;
+ *             it is kept so that split results can be merged.
+ *   causal  : nonzero -> key j is visible to query i iff j <= i (blog 3.4).
+ *   scale   : multiplies Q K^T before the softmax (blog 3.3); finite.
+ *   dtype   : ATTN_DTYPE_F32 (D == 64) or ATTN_DTYPE_BF16 (D == 64 or 128).
+ *   stream  : cudaStream_t or NULL.
+ * Requirements: all pointers non-null and 16-byte aligned; B, H, N >= 1.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int D, int causal, float scale, int dtype,
+             void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode needs.
+ *
+ *   B, Hq, max_blocks_per_seq : as for mla_decode.
+ *   num_sms         : SM count of the device that will run the call
+ *                     (cudaDevAttrMultiProcessorCount); must be >= 2.
+ *   pages_per_split : 0 for the automatic split plan, else the fixed number
+ *                     of 64-token pages per split (see mla_decode_split).
+ * Returns 0 if an argument is invalid.  Pure host arithmetic: no CUDA call.
+ */
+ATTN_API size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_seq,
+                                 int num_sms, int pages_per_split);
+
+/*
+ * mla_decode -- MLA absorbed decode, one query token per sequence.
+ *
+ *   q           : [B, Hq, 576] bf16 absorbed queries [q_nope W_UK | q_rope].
+ *   kv_cache    : [num_blocks, 64, 576] bf16 latent pool; row t of a page is
+ *                 [c_kv (512) | k_rope (64)].  K is the whole row, V is its
+ *                 first 512 entries (the same bytes; nothing is decompressed).
+ *   block_table : [B, max_blocks_per_seq] int32; page j of sequence b lives at
+ *                 kv_cache[block_table[b * max_blocks_per_seq + j]].
+ *   seqlens     : [B] int32, tokens t < seqlens[b] are visible (the single
+ *                 query is the newest token, so no causal mask applies).
+ *   o           : [B, Hq, 512] bf16 (written).
+ *   lse         : [B, Hq] float32 (written); a sequence of length 0 gets
+ *                 o = 0 and lse = -inf.
+ *   scale       : finite multiplier of q . C_t.
+ *   workspace   : device buffer of >= mla_decode_workspace_size(...) bytes,
+ *                 used for the split plan and split partials; 16-byte
+ *                 aligned; contents need not be initialised.  It must not be
+ *                 shared by calls that may run concurrently.
+ * Supported: Hq == 128.  Device-side checks: a block id outside
+ * [0, num_blocks) or a length outside [0, max_blocks_per_seq*64] is never
+ * dereferenced: the affected pages are skipped, the sequence's output is
+ * unspecified, and ATTN_ERR_BAD_BLOCK_TABLE / ATTN_ERR_BAD_SEQLEN is recorded
+ * for attn_device_status().
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.
+ */
+ATTN_API int mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+               const int32_t* seqlens, void* o, float* lse, int B, int Hq,
+               float scale, int max_blocks_per_seq, int num_blocks,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_split -- mla_decode with a fixed split length.
+ *
+ * Identical to mla_decode except that every sequence's pages are cut into
+ * splits of `pages_per_split` 64-token pages along one flat page order
+ * (0 = the automatic plan).  The results agree with mla_decode within
+ * rounding; it exists to exercise the split/merge path at any split count.
+ * The workspace must be sized with the same pages_per_split.
+ */
+ATTN_API int mla_decode_split(const void* q, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seqlens,
+                     void* o, float* lse, int B, int Hq, float scale,
+                     int max_blocks_per_seq, int num_blocks, void* workspace,
+                     size_t workspace_bytes, int pages_per_split,
+                     void* stream);
+
+/*
+ * attn_device_status -- synchronise `stream`, then return and clear the
+ * device error word of the current device (ATTN_OK if no kernel recorded an
+ * error since the last call).  attn_last_error() then names the failing check.
+ */
+ATTN_API int attn_device_status(void* stream);
+
+/* attn_last_error -- thread-local text for the last nonzero return. */
+ATTN_API const char* attn_last_error(void);
+
+/*
+ * attn_fwd_test_skip_load -- TEST HOOK for the bounded-wait failure path.
+ *
+ * Same as attn_fwd with dtype = ATTN_DTYPE_BF16, except that the producer
+ * warp of every CTA deliberately never issues K/V load number
+ * `skip_load_index` (>= 1, counting K0, V0, K1, V1, ...).  The consumers'
+ * bounded waits then run out (about 2 s), the kernel records
+ * ATTN_ERR_DEVICE_TIMEOUT, every CTA unwinds and frees its tensor memory, and
+ * attn_device_status() returns the code.  Nothing hangs, faults or traps.
+ * Output contents are unspecified.  Not for production use.
+ */
+ATTN_API int attn_fwd_test_skip_load(const void* q, const void* k, const void* v,
+                            void* o, float* lse, int B, int H, int N, int D,
+                            int causal, float scale, void* stream,
+                            int skip_load_index);
+
+/*
+ * attn_kv_tiles -- host helper: number of KV tiles of width Bc that the Q
+ * tile `q_tile` (rows [q_tile*Br, q_tile*Br + Br)) visits for sequence
+ * length N.  Causal: kv_limit = min(q_start + Br, N), else N; the count is
+ * ceil(kv_limit / Bc) (blog 3.4).  Returns -1 on invalid arguments.
+ */
+ATTN_API int attn_kv_tiles(int N, int Br, int Bc, int causal, int q_tile);
+
+/*
+ * attn_kernel_info -- host helper: tile shape and dynamic shared memory of
+ * the prefill kernel that attn_fwd launches for (dtype, D): writes Br, Bc,
+ * threads per CTA and shared bytes per CTA.  Returns ATTN_ERR_UNSUPPORTED
+ * for a combination that is not built.
+ */
+ATTN_API int attn_kernel_info(int dtype, int D, int* Br, int* Bc, int* threads,
+                     int* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_ATTN_H_ */

@@ -1,0 +1,226 @@
+"""Python binding of libattn.so (GB300 / sm_103a attention forward).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/attn.h``.  PyTorch is used for
+device memory and streams.  There is no fallback: if the library is missing
+or cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI):
+  attn_fwd(q, k, v, o=None, lse=None, causal=False, scale=None, stream=None)
+  mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None, scale=...,
+             workspace=None, stream=None)
+  mla_decode_split(..., pages_per_split=...)
+  mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms, pages_per_split=0)
+  attn_device_status(stream=None)
+  attn_last_error()
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "AttnError", "lib", "attn_fwd", "mla_decode", "mla_decode_split",
+    "mla_decode_workspace_size", "attn_device_status", "attn_last_error",
+    "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
+    "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_MISALIGNED = -3
+ATTN_ERR_WORKSPACE_TOO_SMALL = -4
+ATTN_ERR_CUDA = -5
+ATTN_ERR_BAD_BLOCK_TABLE = -6
+ATTN_ERR_BAD_SEQLEN = -7
+ATTN_ERR_DEVICE_TIMEOUT = -8
+ATTN_DTYPE_F32 = 0
+ATTN_DTYPE_BF16 = 1
+
+MLA_DK, MLA_DV, MLA_PAGE = 576, 512, 64
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libattn.so not found at {LIB_PATH}: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]
+        L.attn_fwd.restype = _i
+        L.attn_fwd_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                              _f, _vp, _i]
+        L.attn_fwd_test_skip_load.restype = _i
+        L.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.mla_decode_workspace_size.restype = _sz
+        L.mla_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp, _sz,
+                                 _vp]
+        L.mla_decode.restype = _i
+        L.mla_decode_split.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp,
+                                       _sz, _i, _vp]
+        L.mla_decode_split.restype = _i
+        L.attn_device_status.argtypes = [_vp]
+        L.attn_device_status.restype = _i
+        L.attn_last_error.argtypes = []
+        L.attn_last_error.restype = ctypes.c_char_p
+        L.attn_kv_tiles.argtypes = [_i, _i, _i, _i, _i]
+        L.attn_kv_tiles.restype = _i
+        L.attn_kernel_info.argtypes = [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i),
+                                       ctypes.POINTER(_i), ctypes.POINTER(_i)]
+        L.attn_kernel_info.restype = _i
+        _lib = L
+    return _lib
+
+
+def attn_last_error() -> str:
+    return lib().attn_last_error().decode()
+
+
+def _check(code: int):
+    if code != ATTN_OK:
+        raise AttnError(code, attn_last_error())
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _require(t, name, dtype, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def attn_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+             stream=None):
+    """Attention forward. q,k,v: [B,H,N,D] fp32 or bf16 CUDA tensors.
+
+    Returns (o, lse): o like q, lse float32 [B,H,N].
+    """
+    import torch
+    B, H, N, D = q.shape
+    dt = q.dtype
+    if dt == torch.float32:
+        code = ATTN_DTYPE_F32
+    elif dt == torch.bfloat16:
+        code = ATTN_DTYPE_BF16
+    else:
+        raise ValueError(f"unsupported dtype {dt}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, dt, (B, H, N, D))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    _require(o, "o", dt, (B, H, N, D))
+    _require(lse, "lse", torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                          int(bool(causal)), scale, code, _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_fwd_test_skip_load(q, k, v, o, lse, causal: bool, scale: float, skip_load_index: int,
+                            stream=None):
+    """Test hook: bf16 attn_fwd whose producer never issues one K/V load."""
+    B, H, N, D = q.shape
+    _check(lib().attn_fwd_test_skip_load(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                         N, D, int(bool(causal)), float(scale),
+                                         _stream_ptr(stream), int(skip_load_index)))
+
+
+def mla_decode_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_sms: int,
+                              pages_per_split: int = 0) -> int:
+    return int(lib().mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms,
+                                               pages_per_split))
+
+
+def _num_sms(device) -> int:
+    import torch
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def mla_decode_split(q, kv_cache, block_table, seqlens, o=None, lse=None,
+                     scale: float = 1.0 / math.sqrt(192.0), workspace=None,
+                     pages_per_split: int = 0, stream=None):
+    """MLA absorbed decode with an explicit split length (0 = automatic)."""
+    import torch
+    B, Hq, Dk = q.shape
+    _require(q, "q", torch.bfloat16, (B, Hq, MLA_DK))
+    nb, page, dk2 = kv_cache.shape
+    _require(kv_cache, "kv_cache", torch.bfloat16, (nb, MLA_PAGE, MLA_DK))
+    _require(block_table, "block_table", torch.int32)
+    _require(seqlens, "seqlens", torch.int32, (B,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks_per_seq]")
+    max_blocks = block_table.shape[1]
+    if o is None:
+        o = torch.empty(B, Hq, MLA_DV, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, (B, Hq, MLA_DV))
+    _require(lse, "lse", torch.float32, (B, Hq))
+    need = mla_decode_workspace_size(B, Hq, max_blocks, _num_sms(q.device), pages_per_split)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _require(workspace, "workspace", torch.uint8)
+    _check(lib().mla_decode_split(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seqlens),
+                                  _ptr(o), _ptr(lse), B, Hq, float(scale), max_blocks, nb,
+                                  _ptr(workspace), workspace.numel(), int(pages_per_split),
+                                  _stream_ptr(stream)))
+    return o, lse
+
+
+def mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None,
+               scale: float = 1.0 / math.sqrt(192.0), workspace=None, stream=None):
+    """MLA absorbed decode: q [B,128,576] bf16, paged latent pool [nb,64,576] bf16."""
+    return mla_decode_split(q, kv_cache, block_table, seqlens, o, lse, scale, workspace, 0,
+                            stream)
+
+
+def attn_device_status(stream=None, raise_on_error: bool = True) -> int:
+    code = lib().attn_device_status(_stream_ptr(stream))
+    if raise_on_error:
+        _check(code)
+    return code
+
+
+def attn_kv_tiles(N: int, Br: int, Bc: int, causal: bool, q_tile: int) -> int:
+    return lib().attn_kv_tiles(N, Br, Bc, int(bool(causal)), q_tile)
+
+
+def attn_kernel_info(dtype: int, D: int):
+    vals = [ctypes.c_int() for _ in range(4)]
+    _check(lib().attn_kernel_info(dtype, D, *[ctypes.byref(x) for x in vals]))
+    return dict(zip(("Br", "Bc", "threads", "smem_bytes"), (x.value for x in vals)))

@@ -1,0 +1,101 @@
+"""The C ABI library loads on any host and exports what include/attn.h declares.
+
+These checks make no compute call: invalid arguments are rejected by host
+validation before any CUDA call, and the helpers are pure host arithmetic.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import online_softmax_attention_attn_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"^#.*$", "", text, flags=re.M)
+    return sorted(set(re.findall(r"^ATTN_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(pkg.LIB_PATH):
+        from online_softmax_attention_attn_gb300 import _build
+        _build.build()
+    return pkg.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
+              "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
+              "attn_fwd_test_skip_load"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _declared_functions():
+        assert name in exported, f"{name} declared in attn.h but not exported"
+        assert hasattr(L, name)
+
+
+def test_only_the_boundary_is_exported(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {n for n in exported if n.startswith(("attn_", "mla_"))}
+    assert ours == set(_declared_functions())
+
+
+def test_null_pointers_are_rejected_before_any_cuda_call(L):
+    rc = L.attn_fwd(None, None, None, None, None, 1, 1, 16, 64, 0, 0.125, 0, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG
+    assert "null" in pkg.attn_last_error()
+
+
+def test_bad_sizes_dtype_and_head_dim(L):
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    assert L.attn_fwd(p, p, p, p, p, 0, 1, 16, 64, 0, 0.1, 0, None) == pkg.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd(p, p, p, p, p, 1, 1, 16, 64, 0, float("nan"), 0, None) == \
+        pkg.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd(p, p, p, p, p, 1, 1, 16, 96, 0, 0.1, 1, None) == pkg.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fwd(p, p, p, p, p, 1, 1, 16, 128, 0, 0.1, 0, None) == pkg.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fwd(p, p, p, p, p, 1, 1, 16, 64, 0, 0.1, 7, None) == pkg.ATTN_ERR_UNSUPPORTED
+    q = ctypes.c_void_p(24)  # not 16-byte aligned
+    assert L.attn_fwd(q, p, p, p, p, 1, 1, 16, 64, 0, 0.1, 0, None) == pkg.ATTN_ERR_MISALIGNED
+
+
+def test_mla_argument_checks(L):
+    p = ctypes.c_void_p(16)
+    args = [p, p, p, p, p, p]
+    assert L.mla_decode(*args, 1, 128, 0.1, 4, 4, None, 0, None) == pkg.ATTN_ERR_INVALID_ARG
+    assert L.mla_decode(*args, 1, 64, 0.1, 4, 4, p, 1 << 20, None) == pkg.ATTN_ERR_UNSUPPORTED
+    assert L.mla_decode(*args, 0, 128, 0.1, 4, 4, p, 1 << 20, None) == pkg.ATTN_ERR_INVALID_ARG
+    assert L.mla_decode(*args, 1, 128, float("inf"), 4, 4, p, 1 << 20, None) == \
+        pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_workspace_size_is_host_arithmetic(L):
+    assert pkg.mla_decode_workspace_size(0, 128, 64, 152) == 0
+    assert pkg.mla_decode_workspace_size(4, 128, 64, 1) == 0
+    a = pkg.mla_decode_workspace_size(64, 128, 64, 152)
+    b = pkg.mla_decode_workspace_size(64, 128, 64, 152, pages_per_split=1)
+    assert a > 0 and b >= a
+
+
+def test_kernel_info(L):
+    f32 = pkg.attn_kernel_info(pkg.ATTN_DTYPE_F32, 64)
+    assert f32["Br"] == 128 and f32["threads"] == 256
+    bf = pkg.attn_kernel_info(pkg.ATTN_DTYPE_BF16, 128)
+    assert bf["Br"] == 128 and bf["Bc"] == 128 and bf["smem_bytes"] <= 232448
+    with pytest.raises(pkg.AttnError):
+        pkg.attn_kernel_info(pkg.ATTN_DTYPE_F32, 80)

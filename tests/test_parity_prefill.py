@@ -1,0 +1,137 @@
+"""GPU parity of attn_fwd (fp32 and bf16 paths) against the fp64 oracle.
+
+Element-by-element on small and ragged shapes that span several tiles; at the
+full workload sizes on sampled rows the oracle computes one by one, plus
+properties that hold at any size (finite, convex combination of V rows).
+Tolerances: fp32 path O and LSE within 1e-4; bf16 path O within 2e-2 and
+LSE within 1e-3 (max abs error against the unrounded fp64 oracle).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_softmax_attention_attn_gb300 as pkg
+from online_softmax_attention_attn_gb300.inputs import (BF16_PREFILL, FP32_PAGE2,
+                                                         FP32_SMALL_CAUSAL, mha_inputs,
+                                                         mha_config_inputs)
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: (1e-4, 1e-4), torch.bfloat16: (2e-2, 1e-3)}
+
+
+def _run(q, k, v, causal, scale):
+    dev = torch.device("cuda")
+    o, lse = pkg.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    pkg.attn_device_status()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check_full(q, k, v, causal, scale):
+    o, lse = _run(q, k, v, causal, scale)
+    ro, rl = oracle.mha(q, k, v, causal, scale)
+    to, tl = TOL[q.dtype]
+    eo, el = np.abs(o - ro).max(), np.abs(lse - rl).max()
+    assert eo <= to and el <= tl, f"O err {eo:.3g}, LSE err {el:.3g}"
+    return eo, el
+
+
+def _sample_rows(B, H, N, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for bh in (0, B * H - 1):
+        for i in (0, 1, 127, 128, N // 2, N - 129, N - 128, N - 1):
+            if 0 <= i < N:
+                rows.add(bh * N + i)
+    rows.update(rng.integers(0, B * H * N, size=n).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _check_sampled(q, k, v, causal, scale, o, lse, nrows=384, seed=0):
+    B, H, N, D = q.shape
+    rows = _sample_rows(B, H, N, nrows, seed)
+    ro, rl = oracle.mha(q, k, v, causal, scale, rows=rows)
+    go = o.reshape(-1, D)[rows]
+    gl = lse.reshape(-1)[rows]
+    to, tl = TOL[q.dtype]
+    eo, el = np.abs(go - ro).max(), np.abs(gl - rl).max()
+    assert eo <= to and el <= tl, f"O err {eo:.3g}, LSE err {el:.3g}"
+    # properties at every row: finite, and O inside the hull of the V rows
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    vmin = v.float().amin(dim=2).numpy()[:, :, None, :]
+    vmax = v.float().amax(dim=2).numpy()[:, :, None, :]
+    slack = to
+    assert (o.reshape(B, H, N, D) >= vmin - slack).all()
+    assert (o.reshape(B, H, N, D) <= vmax + slack).all()
+
+
+# ------------------------------------------------------------------ fp32
+
+def test_fp32_small_causal_workload():
+    cfg = FP32_SMALL_CAUSAL
+    q, k, v = mha_config_inputs(cfg)
+    _check_full(q, k, v, cfg.causal, cfg.scale)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 7, 64, 200, 321])
+def test_fp32_ragged(N, causal):
+    q, k, v = mha_inputs(2, 3, N, 64, torch.float32, seed=200 + N)
+    _check_full(q, k, v, causal, 0.125)
+
+
+def test_fp32_scale_zero_gives_prefix_means():
+    q, k, v = mha_inputs(1, 2, 300, 64, torch.float32, seed=5)
+    o, lse = _run(q, k, v, True, 0.0)
+    ref = (torch.cumsum(v.double(), 2) / torch.arange(1, 301).double()[None, None, :, None])
+    assert np.abs(o - ref.numpy()).max() <= 1e-5
+    assert np.abs(lse - np.log(np.arange(1, 301))[None, None]).max() <= 1e-5
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_page2_workload_sampled(causal):
+    cfg = FP32_PAGE2
+    q, k, v = mha_config_inputs(cfg)
+    o, lse = _run(q, k, v, causal, cfg.scale)
+    _check_sampled(q, k, v, causal, cfg.scale, o, lse, seed=int(causal))
+
+
+# ------------------------------------------------------------------ bf16
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 100, 128, 256, 300, 513])
+def test_bf16_d128_small_and_ragged(N, causal):
+    q, k, v = mha_inputs(2, 2, N, 128, torch.bfloat16, seed=300 + N)
+    _check_full(q, k, v, causal, 1.0 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [64, 256, 389])
+def test_bf16_d64(N, causal):
+    q, k, v = mha_inputs(2, 3, N, 64, torch.bfloat16, seed=400 + N)
+    _check_full(q, k, v, causal, 0.125)
+
+
+def test_bf16_long_rows_exercise_lazy_rescale():
+    """Scores with a growing trend force the running max up many times."""
+    B, H, N, D = 1, 2, 1024, 128
+    q, k, v = mha_inputs(B, H, N, D, torch.float32, seed=9)
+    k = k + torch.linspace(0, 6, N)[None, None, :, None] * q.mean(2, keepdim=True).sign()
+    _check_full(q.bfloat16(), k.bfloat16(), v.bfloat16(), True, 0.5)
+
+
+def test_bf16_prefill_workload_sampled():
+    cfg = BF16_PREFILL
+    q, k, v = mha_config_inputs(cfg)
+    o, lse = _run(q, k, v, cfg.causal, cfg.scale)
+    _check_sampled(q, k, v, cfg.causal, cfg.scale, o, lse, nrows=512, seed=3)
+
+
+def test_bf16_repeat_calls_are_bitwise_identical():
+    q, k, v = mha_inputs(2, 4, 700, 128, torch.bfloat16, seed=11)
+    a = _run(q, k, v, True, 0.09)
+    b = _run(q, k, v, True, 0.09)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
