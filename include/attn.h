@@ -144,6 +144,41 @@ ATTN_API int mla_decode_split(const void* q, const void* kv_cache,
                      void* stream);
 
 /*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
+ * memory when they call.
+ *
+ * The pages this library follows have no counterpart to this entry point.
+ * It exists for callers that are not allowed to allocate device memory at
+ * call time: for example a host that hands all free device memory to its
+ * own pool up front and forbids later cudaMalloc, or a caller on a path that
+ * must not pay for the allocator (cudaMalloc / cudaFree can synchronise the
+ * device).  Such callers cannot provide mla_decode's workspace.
+ *
+ * Arguments and results are those of mla_decode minus the workspace; the
+ * automatic split plan is used.  The plan and the split partials live in
+ * one fixed array inside libattn.so (a file-scope static __device__ array of
+ * 42,057,984 bytes, about 40.1 MiB), which every GPU that loads the library
+ * keeps until the process exits.
+ *   Limits: B <= 8192 sequences and a device of at most 160 SMs; beyond
+ *   them the call returns ATTN_ERR_UNSUPPORTED and launches nothing.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current) and caches it;
+ *   make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and the array keeps
+ *   the last call's contents (each call rewrites everything it reads).  Calls
+ *   that can overlap on the GPU -- on unordered streams or from several host
+ *   threads -- race on it; the caller must serialise them.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+ATTN_API int mla_decode_noalloc(const void* q, const void* kv_cache,
+                                const int32_t* block_table,
+                                const int32_t* seqlens, void* o, float* lse,
+                                int B, int Hq, float scale,
+                                int max_blocks_per_seq, int num_blocks,
+                                void* stream);
+
+/*
  * attn_device_status -- synchronise `stream`, then return and clear the
  * device error word of the current device (ATTN_OK if no kernel recorded an
  * error since the last call).  attn_last_error() then names the failing check.

@@ -22,7 +22,7 @@ import os
 
 __all__ = [
     "AttnError", "lib", "attn_fwd", "mla_decode", "mla_decode_split",
-    "mla_decode_workspace_size", "attn_device_status", "attn_last_error",
+    "mla_decode_workspace_size", "mla_decode_noalloc", "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
     "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
 ]
@@ -77,6 +77,8 @@ def lib():
         L.mla_decode_split.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp,
                                        _sz, _i, _vp]
         L.mla_decode_split.restype = _i
+        L.mla_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp]
+        L.mla_decode_noalloc.restype = _i
         L.attn_device_status.argtypes = [_vp]
         L.attn_device_status.restype = _i
         L.attn_last_error.argtypes = []
@@ -207,6 +209,33 @@ def mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None,
     """MLA absorbed decode: q [B,128,576] bf16, paged latent pool [nb,64,576] bf16."""
     return mla_decode_split(q, kv_cache, block_table, seqlens, o, lse, scale, workspace, 0,
                             stream)
+
+
+def mla_decode_noalloc(q, kv_cache, block_table, seqlens, o=None, lse=None,
+                       scale: float = 1.0 / math.sqrt(192.0), stream=None):
+    """MLA decode without a workspace: the library's fixed device scratch is used.
+
+    For callers that may not allocate device memory when they call; o and lse
+    must then be passed in.  Calls that can overlap on the GPU share the one
+    scratch array and must be serialised by the caller.
+    """
+    import torch
+    B, Hq, _ = q.shape
+    _require(q, "q", torch.bfloat16, (B, Hq, MLA_DK))
+    nb = kv_cache.shape[0]
+    _require(kv_cache, "kv_cache", torch.bfloat16, (nb, MLA_PAGE, MLA_DK))
+    _require(block_table, "block_table", torch.int32)
+    _require(seqlens, "seqlens", torch.int32, (B,))
+    if o is None:
+        o = torch.empty(B, Hq, MLA_DV, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.bfloat16, (B, Hq, MLA_DV))
+    _require(lse, "lse", torch.float32, (B, Hq))
+    _check(lib().mla_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(block_table),
+                                    _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, float(scale),
+                                    block_table.shape[1], nb, _stream_ptr(stream)))
+    return o, lse
 
 
 def attn_device_status(stream=None, raise_on_error: bool = True) -> int:

@@ -214,6 +214,32 @@ extern "C" int mla_decode_split(const void* q, const void* kv_cache,
                   num_blocks, workspace, workspace_bytes, pages_per_split, stream);
 }
 
+extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache,
+                                  const int32_t* block_table, const int32_t* seqlens,
+                                  void* o, float* lse, int B, int Hq, float scale,
+                                  int max_blocks_per_seq, int num_blocks, void* stream) {
+  g_msg[0] = '\0';
+  if (B > mla_noalloc_max_batch())
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "mla_decode_noalloc: B=%d exceeds the fixed-scratch limit of %d sequences", B,
+                mla_noalloc_max_batch());
+  int code = ATTN_OK;
+  const int nsm = sm_count(&code);
+  if (nsm <= 0) return code;
+  if (nsm > mla_noalloc_max_sms())
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "mla_decode_noalloc: device has %d SMs, the fixed scratch covers %d", nsm,
+                mla_noalloc_max_sms());
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  cudaError_t e = mla_noalloc_scratch(&ws, &ws_bytes);
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, "mla_decode_noalloc: cudaGetSymbolAddress failed: %s",
+                cudaGetErrorString(e));
+  return mla_impl(q, kv_cache, block_table, seqlens, o, lse, B, Hq, scale, max_blocks_per_seq,
+                  num_blocks, ws, ws_bytes, 0, stream);
+}
+
 // ---------------------------------------------------------------- status
 
 extern "C" int attn_device_status(void* stream) {

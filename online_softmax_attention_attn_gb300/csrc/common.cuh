@@ -123,6 +123,11 @@ bool prefill_f32_info(int D, int* Br, int* Bc, int* threads, int* smem);
 bool prefill_bf16_info(int D, int* Br, int* Bc, int* threads, int* smem);
 size_t mla_workspace_bytes(int B, int Hq, int max_blocks, int num_sms, int pages_per_split);
 
+// Fixed-scratch support for mla_decode_noalloc (defined in mla_decode.cu).
+cudaError_t mla_noalloc_scratch(void** ptr, size_t* bytes);
+int mla_noalloc_max_batch();
+int mla_noalloc_max_sms();
+
 // Error-message helper shared by the host files.
 void attn_set_error(const char* fmt, ...);
 

@@ -31,6 +31,8 @@
 //   * Every wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -71,10 +73,10 @@ struct WsLayout {
   int max_slots;
 };
 
-__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WsLayout ws_layout(int B, int max_slots) {
-  WsLayout w;
+__host__ __device__ constexpr WsLayout ws_layout(int B, int max_slots) {
+  WsLayout w{};
   w.max_slots = max_slots;
   w.header = 0;
   w.prefix = 64;
@@ -695,4 +697,47 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   mla_combine_kernel<<<dim3(a.B, kHq / 16), 256, 0, s>>>(hdr, prefix, plse, po,
                                                          static_cast<__nv_bfloat16*>(a.o), a.lse);
   return cudaGetLastError();
+}
+
+// ---- fixed scratch for callers that cannot allocate ---------------------------
+// mla_decode_noalloc runs the same plan / decode / combine kernels with the
+// workspace placed in this file-scope device array instead of a caller
+// buffer.  Its size covers the automatic plan for up to kNoAllocMaxBatch
+// sequences on a device of up to kNoAllocMaxSms SMs (2 partial slots per
+// 2-SM cluster).  Every GPU that loads the library reserves it until exit.
+namespace {
+constexpr int kNoAllocMaxBatch = 8192;
+constexpr int kNoAllocMaxSms = 160;
+constexpr size_t kNoAllocScratchBytes =
+    ws_layout(kNoAllocMaxBatch, 2 * (kNoAllocMaxSms / 2)).total;
+static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size");
+
+static __device__ __align__(256) uint8_t g_mla_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevs = 64;
+void* g_scratch_addr[kMaxDevs] = {};
+std::mutex g_scratch_mu;
+}  // namespace
+
+int mla_noalloc_max_batch() { return kNoAllocMaxBatch; }
+int mla_noalloc_max_sms() { return kNoAllocMaxSms; }
+
+// Device address of the fixed scratch on the current device.  The symbol's
+// host-side name is only a stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+cudaError_t mla_noalloc_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevs) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mla_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *ptr = g_scratch_addr[dev];
+  *bytes = kNoAllocScratchBytes;
+  return cudaSuccess;
 }
