@@ -276,6 +276,8 @@ class DecodeLeg:
 def make_leg(name, dev):
     if name == "prefill":
         return PrefillLeg(I.BF16_PREFILL, dev)
+    if name == "prefill_noncausal":
+        return PrefillLeg(I.BF16_PREFILL_NONCAUSAL, dev)
     if name == "fp32":
         return PrefillLeg(I.FP32_PAGE2, dev)
     if name == "fp32_causal":
@@ -366,9 +368,9 @@ def make_leg_cpu(name):
             self.q, self.kv, self.table, self.sl = I.mla_config_inputs(cfg)
             self.bytes = metrics.mla_bytes(self.sl.tolist(), cfg.Hq,
                                            max_blocks=self.table.shape[1])
-    if name in ("prefill", "fp32", "fp32_causal"):
-        cfg = {"prefill": I.BF16_PREFILL, "fp32": I.FP32_PAGE2,
-               "fp32_causal": I.FP32_PAGE2_CAUSAL}[name]
+    if name in ("prefill", "prefill_noncausal", "fp32", "fp32_causal"):
+        cfg = {"prefill": I.BF16_PREFILL, "prefill_noncausal": I.BF16_PREFILL_NONCAUSAL,
+               "fp32": I.FP32_PAGE2, "fp32_causal": I.FP32_PAGE2_CAUSAL}[name]
         return _P(cfg)
     return _D(I.MLA_B64 if name == "decode" else I.MLA_B256_PAGED)
 
@@ -406,7 +408,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="step",
-                    choices=["step", "prefill", "decode", "decode_paged", "fp32", "fp32_causal"])
+                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged", "fp32",
+                             "fp32_causal"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

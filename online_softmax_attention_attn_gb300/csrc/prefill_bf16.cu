@@ -2,7 +2,7 @@
 // cores (tcgen05 + TMEM), sm_103a.
 //
 // What it computes is the FlashAttention-2 forward of the "FP32 CUDA-core
-// FlashAttention-2 v2" blog (dandandamowang post_1787450400): one Q block is
+// FlashAttention-2 v2" blog (dandandamowang post_1787450400): Q blocks are
 // resident for the whole KV loop (section 1.2), K/V blocks stream through a
 // multi-stage buffer (section 3.2), the softmax is online with a deferred 1/l
 // (sections 1.3, 3.3, 3.5), blocks above the causal diagonal are skipped and
@@ -11,20 +11,25 @@
 // suggests (fp32 -> bf16 conversion of P).
 //
 // How it maps onto GB300 (nothing here is taken from the pages' Ampere,
-// Hopper or RTX kernels):
-//   * warp 4  : TMA producer.  Q once, then K_j, V_j into a ring of 32 KB
-//               slots (128-byte swizzle), full/empty mbarriers per slot.
-//   * warp 5  : MMA issuer (one thread) and TMEM owner.  S_j = Q K_j^T is a
-//               tcgen05.mma M=128, N=128, K=D into one of two TMEM S buffers;
-//               O += P_j V_j takes P straight from TMEM (the A operand) and V
-//               from shared memory, accumulating in TMEM.
-//   * warps 0-3: softmax, one thread per query row (TMEM lane = row): load the
-//               S row, mask, running max, exp2, row sum, write P (bf16) into
-//               the S buffer's columns, rescale O in TMEM only when the max
-//               grew by more than 2^8 (lazy rescale; exact because O and l
-//               share the stale reference), and finally O/l -> bf16 -> smem ->
-//               TMA store, plus LSE.
-//   TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+// Hopper or RTX kernels).  One CTA owns TWO consecutive 128-row Q tiles of
+// one head and streams that head's K/V blocks once for both:
+//   * warp 8  : TMA producer.  Both Q tiles once, then K_j, V_j into a ring of
+//               32 KB slots (128-byte swizzle), full/empty mbarriers per slot.
+//   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
+//               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
+//               O_t += P_t V_j with P read straight from TMEM as the A operand.
+//               The issue order S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, ... lets
+//               the tensor core work on one tile while the other tile's
+//               softmax runs (ping-pong).
+//   * warps 0-3 / 4-7 : softmax warpgroup of tile 0 / tile 1, one thread per
+//               query row (TMEM lane = row): load the S row, mask, running max,
+//               exp2, row sum, write P (bf16) over the S columns, rescale O in
+//               TMEM only when the max grew by more than 2^8 (lazy rescale;
+//               exact because O and l share the stale reference), and finally
+//               O/l -> bf16 -> smem -> TMA store, plus LSE.
+//   TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
+//   Work order: heads in groups of 16 (the CTAs running together share those
+//   heads' K/V in L2), heaviest causal Q pairs first within a group.
 //   Every wait is bounded (about 2 s); a stuck pipeline records
 //   ATTN_ERR_DEVICE_TIMEOUT and the CTA unwinds, frees TMEM and exits.
 #include <math.h>
@@ -35,28 +40,30 @@ namespace {
 
 using namespace gb300;
 
-constexpr int kBM = 128;              // query rows per CTA
+constexpr int kBM = 128;              // query rows per Q tile
 constexpr int kBN = 128;              // keys per KV block
-constexpr int kThreads = 192;         // 4 softmax warps + producer + MMA
+constexpr int kTilesPerCta = 2;
+constexpr int kThreads = 320;         // 2 softmax warpgroups + producer + MMA
 constexpr int kAtomBytes = 128 * 128; // one 128-row x 64-col bf16 swizzle column
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kHeadGroup = 16;             // heads scheduled together
 
 template <int D>
 struct Cfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kTileBytes = kAtoms * kAtomBytes;  // Q, K or V block
-  static constexpr int kStages = (D == 128) ? 5 : 8;      // ring slots
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kStages = (D == 128) ? 5 : 10;     // ring slots
+  static constexpr int kQOff = 0;                          // Q0, Q1
+  static constexpr int kRingOff = kTilesPerCta * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done,
-  // mma_drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+  // pv_done[2], mma_drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS0 = 0;
-  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColS = 0;    // + 128 * tile
+  static constexpr uint32_t kColO = 256;  // + 128 * tile
 };
 
 template <int D, bool kCausal>
@@ -79,37 +86,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_q_full = bar0;
   auto bar_kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_kv_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
-  auto bar_s_full = [&](int b) { return bar0 + 8u * (1 + 2 * C::kStages + b); };
-  auto bar_p_full = [&](int b) { return bar0 + 8u * (3 + 2 * C::kStages + b); };
-  const uint32_t bar_pv_done = bar0 + 8u * (5 + 2 * C::kStages);
-  const uint32_t bar_mma_drain = bar0 + 8u * (6 + 2 * C::kStages);
+  auto bar_s_full = [&](int t) { return bar0 + 8u * (1 + 2 * C::kStages + t); };
+  auto bar_p_full = [&](int t) { return bar0 + 8u * (3 + 2 * C::kStages + t); };
+  auto bar_pv_done = [&](int t) { return bar0 + 8u * (5 + 2 * C::kStages + t); };
+  const uint32_t bar_mma_drain = bar0 + 8u * (7 + 2 * C::kStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: heaviest causal Q blocks first across all heads
+  // ---- work item: heads in groups of kHeadGroup (their K/V stay in L2);
+  // within a group, heaviest causal Q pairs first across the group's heads.
   const int n_qt = (N + kBM - 1) / kBM;
-  const int lin = blockIdx.x;
-  const int qt = kCausal ? (n_qt - 1 - lin / BH) : (lin / BH);
-  const int bh = lin % BH;
-  const int q0 = qt * kBM;
-  const int kv_limit = kCausal ? min(q0 + kBM, N) : N;
-  const int T = (kv_limit + kBN - 1) / kBN;  // KV blocks visited
+  const int n_pairs = (n_qt + 1) / 2;
+  const int group = blockIdx.x / (kHeadGroup * n_pairs);
+  const int g_heads = min(kHeadGroup, BH - group * kHeadGroup);
+  const int rem = blockIdx.x - group * kHeadGroup * n_pairs;
+  const int bh = group * kHeadGroup + rem % g_heads;
+  const int pr = kCausal ? (n_pairs - 1 - rem / g_heads) : (rem / g_heads);
+  int Tt[kTilesPerCta];  // KV blocks visited by each Q tile (0: tile absent)
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int qt = 2 * pr + t;
+    if (qt >= n_qt) {
+      Tt[t] = 0;
+    } else {
+      const int kv_limit = kCausal ? min(qt * kBM + kBM, N) : N;
+      Tt[t] = (kv_limit + kBN - 1) / kBN;
+    }
+  }
+  const int ntiles = Tt[1] > 0 ? 2 : 1;
+  const int Tmax = max(Tt[0], Tt[1]);
 
-  // ---- setup: barriers (thread 0), TMEM (warp 5)
+  // ---- setup: barriers (thread 0), TMEM (warp 9)
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s_full(b), 1);
-      mbar_init(bar_p_full(b), 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s_full(t), 1);
+      mbar_init(bar_p_full(t), 128);
+      mbar_init(bar_pv_done(t), 1);
     }
-    mbar_init(bar_pv_done, 1);
     mbar_init(bar_mma_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -118,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmO);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -127,16 +148,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ================= TMA producer =================
     if (lane == 0) {
-      const uint64_t pol_kv = policy_evict_last();  // K/V are re-read by other Q blocks
-      mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
-      for (int a = 0; a < C::kAtoms; ++a)
-        tma_load_3d(sQ + a * kAtomBytes, &tmQ, bar_q_full, a * 64, q0, bh);
+      const uint64_t pol_kv = policy_evict_last();  // K/V are re-read by the head's other CTAs
+      mbar_arrive_expect_tx(bar_q_full, ntiles * C::kTileBytes);
+      for (int t = 0; t < ntiles; ++t)
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full, a * 64,
+                      (2 * pr + t) * kBM, bh);
       int issued_until = 0;  // loads [0, issued_until) were issued
       bool ok = true;
-      for (int idx = 0; idx < 2 * T && ok; ++idx) {
+      for (int idx = 0; idx < 2 * Tmax && ok; ++idx) {
         const int slot = idx % C::kStages;
         const int use = idx / C::kStages;
         if (use > 0) {
@@ -159,69 +182,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first = issued_until > C::kStages ? issued_until - C::kStages : 0;
         for (int idx = first; idx < issued_until; ++idx) {
           if (debug_skip_load > 0 && idx == debug_skip_load) continue;
-          const int slot = idx % C::kStages;
           volatile int never = 0;
-          mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, &never, nullptr, kSiteDrain,
-                    idx);
+          mbar_wait(bar_kv_full(idx % C::kStages), (idx / C::kStages) & 1, &never, nullptr,
+                    kSiteDrain, idx);
         }
         volatile int never = 0;
         mbar_wait(bar_q_full, 0, &never, nullptr, kSiteDrain, -1);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ================= MMA issuer =================
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
-      const uint32_t tS = tbase + C::kColS0;
-      const uint32_t tO = tbase + C::kColO;
       bool ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
       tc_fence_after();
 
-      auto issue_s = [&](int j) -> bool {
+      // S_t = Q_t K_j^T; the slot of K_j is released by the last tile using it.
+      auto issue_s = [&](int t, int j) -> bool {
         const int idx = 2 * j;
         const int slot = idx % C::kStages;
         if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
                        kSiteKvFull, idx))
           return false;
         tc_fence_after();
+        const uint32_t qb = sQ + t * C::kTileBytes;
         const uint32_t kb = sRing + slot * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_ss(tS + (j & 1) * 128, sdesc_sw128(sQ + off, 16, 1024),
+          mma_ss(tbase + C::kColS + t * 128, sdesc_sw128(qb + off, 16, 1024),
                  sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
         }
-        tc_commit(bar_kv_empty(slot));
-        tc_commit(bar_s_full(j & 1));
+        tc_commit(bar_s_full(t));
+        const int last_t = (j < Tt[1]) ? 1 : 0;
+        if (t == last_t) tc_commit(bar_kv_empty(slot));
         return true;
       };
-
-      if (ok) ok = issue_s(0);
-      if (ok && T > 1) ok = issue_s(1);
-      for (int j = 0; j < T && ok; ++j) {
-        ok = mbar_wait(bar_p_full(j & 1), (j >> 1) & 1, abort_flag, err, kSitePFull, j);
-        if (!ok) break;
+      // O_t += P_t V_j once the softmax of tile t has written P_t.
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!mbar_wait(bar_p_full(t), j & 1, abort_flag, err, kSitePFull, j)) return false;
         tc_fence_after();
         const int idx = 2 * j + 1;
         const int slot = idx % C::kStages;
-        ok = mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
-                       kSiteKvFull, idx);
-        if (!ok) break;
+        if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
+                       kSiteKvFull, idx))
+          return false;
         tc_fence_after();
         const uint32_t vb = sRing + slot * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
           // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
-          mma_ts(tO, tS + (j & 1) * 128 + kk * 8,
+          mma_ts(tbase + C::kColO + t * 128, tbase + C::kColS + t * 128 + kk * 8,
                  sdesc_sw128(vb + kk * 16 * 128, kAtomBytes, 1024), kIdescPV,
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(bar_kv_empty(slot));
-        tc_commit(bar_pv_done);
-        if (j + 2 < T) ok = issue_s(j + 2);
+        tc_commit(bar_pv_done(t));
+        const int last_t = (j < Tt[1]) ? 1 : 0;
+        if (t == last_t) tc_commit(bar_kv_empty(slot));
+        return true;
+      };
+
+      for (int t = 0; t < kTilesPerCta && ok; ++t)
+        if (Tt[t] > 0) ok = issue_s(t, 0);
+      for (int j = 0; j < Tmax && ok; ++j) {
+        for (int t = 0; t < kTilesPerCta && ok; ++t) {
+          if (j >= Tt[t]) continue;
+          ok = issue_pv(t, j);
+          if (ok && j + 1 < Tt[t]) ok = issue_s(t, j + 1);
+        }
       }
       // Every MMA this thread issued must be complete before TMEM is freed.
       tc_commit(bar_mma_drain);
@@ -230,37 +261,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ================= softmax + correction + epilogue (warps 0-3) =========
-    const int r = threadIdx.x;  // row within the Q block == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tbase + lane_off + C::kColS0;
-    const uint32_t tO = tbase + lane_off + C::kColO;
+    // ================= softmax warpgroups (tile t = warp / 4) ==============
+    const int t = warp >> 2;
+    const int T = Tt[t];
+    const int r = threadIdx.x & 127;  // row within the Q tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + C::kColS + t * 128;
+    const uint32_t tO = tbase + lane_off + C::kColO + t * 128;
+    const int q0 = (2 * pr + t) * kBM;
     const int row = q0 + r;
-    // keys [0, lim) are visible to this row
-    const int lim = kCausal ? min(N, row + 1) : N;
+    const int lim = kCausal ? min(N, row + 1) : N;  // keys [0, lim) are visible
     float m_ref = -INFINITY;  // running max (log2 units), lazily updated
     float l = 0.f;
     bool ok = true;
 
     for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(bar_s_full(j & 1), (j >> 1) & 1, abort_flag, err, kSiteSFull, j);
+      ok = mbar_wait(bar_s_full(t), j & 1, abort_flag, err, kSiteSFull, j);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
       float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + (j & 1) * 128 + c * 32, s + c * 32);
+      tmem_ld128(tS, s);
 
-      const int kv0 = j * kBN;
-      const int nvalid = lim - kv0;  // keys k < nvalid of this block are visible
-      float mt = -INFINITY;
-      if (nvalid >= kBN) {
+      const int nvalid = lim - j * kBN;  // keys k < nvalid of this block are visible
+      const bool full = nvalid >= kBN;
+      float mt;
+      if (full) {
+        // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
+        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+        if (scale_log2 >= 0.f) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] *= scale_log2;
-          mt = fmaxf(mt, s[c]);
+          for (int c = 4; c < kBN; c += 4) {
+            a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
+            a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
+          }
+          mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+        } else {
+#pragma unroll
+          for (int c = 4; c < kBN; c += 4) {
+            a0 = fminf(a0, s[c]); a1 = fminf(a1, s[c + 1]);
+            a2 = fminf(a2, s[c + 2]); a3 = fminf(a3, s[c + 3]);
+          }
+          mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
         }
       } else {
+        mt = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
           s[c] = (c < nvalid) ? s[c] * scale_log2 : -INFINITY;
@@ -276,23 +321,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint32_t p[kBN / 2];
-      float rs = 0.f;
+      // P = 2^(t - m), packed to bf16 pairs and written over the S columns
+      // in two halves of 64 keys (32 TMEM columns each).
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = fast_exp2(s[c] - m_use);
-        const float p1 = fast_exp2(s[c + 1] - m_use);
-        rs += p0 + p1;
-        p[c / 2] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t p[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const int k = h * 64 + c;
+          float p0, p1, p2, p3;
+          if (full) {
+            p0 = fast_exp2(fmaf(s[k], scale_log2, -m_use));
+            p1 = fast_exp2(fmaf(s[k + 1], scale_log2, -m_use));
+            p2 = fast_exp2(fmaf(s[k + 2], scale_log2, -m_use));
+            p3 = fast_exp2(fmaf(s[k + 3], scale_log2, -m_use));
+          } else {
+            p0 = fast_exp2(s[k] - m_use);
+            p1 = fast_exp2(s[k + 1] - m_use);
+            p2 = fast_exp2(s[k + 2] - m_use);
+            p3 = fast_exp2(s[k + 3] - m_use);
+          }
+          r0 += p0; r1 += p1; r2 += p2; r3 += p3;
+          p[c / 2] = pack_bf16x2(p0, p1);
+          p[c / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(tS + h * 32, p);
       }
-      l += rs;
-#pragma unroll
-      for (int c = 0; c < kBN / 64; ++c) tmem_st32(tS + (j & 1) * 128 + c * 32, p + c * 32);
+      l += (r0 + r1) + (r2 + r3);
 
       // Lazy correction of O: needed only if some row of this warp moved its
       // reference, and only once PV_{j-1} has landed in TMEM.
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        ok = mbar_wait(bar_pv_done, (j - 1) & 1, abort_flag, err, kSitePvDone, j);
+        ok = mbar_wait(bar_pv_done(t), (j - 1) & 1, abort_flag, err, kSitePvDone, j);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -302,59 +363,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tO + c * 32, ov);
           uint32_t ou[32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) ou[t] = __float_as_uint(ov[t] * alpha);
+          for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
           tmem_st32(tO + c * 32, ou);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p_full(j & 1));
+      mbar_arrive(bar_p_full(t));
     }
 
-    if (ok) ok = mbar_wait(bar_pv_done, (T - 1) & 1, abort_flag, err, kSitePvDone, T);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      // ---- epilogue: O / l -> bf16 into the (now free) Q buffer, TMA store
-      const float inv_l = 1.0f / l;
-      uint8_t* stage = smem + C::kQOff;
+    if (T > 0) {
+      if (ok) ok = mbar_wait(bar_pv_done(t), (T - 1) & 1, abort_flag, err, kSitePvDone, T);
+      ok = __all_sync(0xffffffffu, ok);
+      const uint32_t stage_addr = sQ + t * C::kTileBytes;  // Q_t is no longer read
+      if (ok) {
+        tc_fence_after();
+        // ---- epilogue: O / l -> bf16 into the Q_t buffer, then TMA store
+        const float inv_l = 1.0f / l;
+        uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tmem_ld32(tO + c * 32, ov);
-        const int atom = (c * 32) / 64;
-        const int chunk0 = ((c * 32) % 64) / 8;  // 16-byte chunk within the 128-B row
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          const int atom = (c * 32) / 64;
+          const int chunk0 = ((c * 32) % 64) / 8;  // 16-byte chunk within the 128-B row
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w;
-          w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
-          w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
-          w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
-          w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
-          const int phys = (chunk0 + q4) ^ (r & 7);  // 128-byte swizzle
-          *reinterpret_cast<uint4*>(stage + atom * kAtomBytes + r * 128 + phys * 16) = w;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
+            w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
+            w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
+            w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
+            const int phys = (chunk0 + q4) ^ (r & 7);  // 128-byte swizzle
+            *reinterpret_cast<uint4*>(stage + atom * kAtomBytes + r * 128 + phys * 16) = w;
+          }
+        }
+        fence_proxy_async_smem();
+        if (row < N) {
+          constexpr float kLn2 = 0.69314718055994530942f;
+          lse[(size_t)bh * N + row] = (m_ref + log2f(l)) * kLn2;
         }
       }
-      fence_proxy_async_smem();
-      if (row < N) {
-        constexpr float kLn2 = 0.69314718055994530942f;
-        lse[(size_t)bh * N + row] = (m_ref + log2f(l)) * kLn2;
+      // All four warps of this warpgroup reach this barrier on every path
+      // (their waits are bounded); the store is skipped if any role aborted.
+      named_barrier_sync(1 + t, 128);
+      if (r == 0 && *abort_flag == 0) {
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_store_3d(&tmO, stage_addr + a * kAtomBytes, a * 64, q0, bh);
+        bulk_commit();
+        bulk_wait_all();
       }
-    }
-    // All four softmax warps reach this barrier on every path (their waits
-    // are bounded); the store is skipped if any role aborted.
-    named_barrier_sync(1, 128);
-    if (threadIdx.x == 0 && *abort_flag == 0) {
-      for (int a = 0; a < C::kAtoms; ++a) tma_store_3d(&tmO, sQ + a * kAtomBytes, a * 64, q0, bh);
-      bulk_commit();
-      bulk_wait_all();
     }
   }
 
   // ---- teardown: every role has finished (or unwound); free TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
   }
@@ -372,6 +437,11 @@ CUresult make_map_3d(CUtensorMap* map, const void* ptr, int D, int N, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+long long num_ctas(int B, int H, int N) {
+  const int n_qt = (N + kBM - 1) / kBM;
+  return (long long)((n_qt + 1) / 2) * B * H;
+}
+
 template <int D, bool kCausal>
 cudaError_t launch_t(const PrefillBf16Args& a, const CUtensorMap& mq, const CUtensorMap& mk,
                      const CUtensorMap& mv, const CUtensorMap& mo, cudaStream_t s) {
@@ -380,11 +450,9 @@ cudaError_t launch_t(const PrefillBf16Args& a, const CUtensorMap& mq, const CUte
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int BH = a.B * a.H;
-  const long long blocks = (long long)((a.N + kBM - 1) / kBM) * BH;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<(unsigned)blocks, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mo, a.lse, BH, a.N,
-                                                          scale_log2, a.err, a.debug_skip_load);
+  kern<<<(unsigned)num_ctas(a.B, a.H, a.N), kThreads, C::kSmemBytes, s>>>(
+      mq, mk, mv, mo, a.lse, a.B * a.H, a.N, scale_log2, a.err, a.debug_skip_load);
   return cudaGetLastError();
 }
 
@@ -403,12 +471,12 @@ bool prefill_bf16_info(int D, int* Br, int* Bc, int* threads, int* smem) {
 }
 
 cudaError_t launch_prefill_bf16(const PrefillBf16Args& a, cudaStream_t s) {
-  const int BH = a.B * a.H;
-  const long long blocks = (long long)((a.N + kBM - 1) / kBM) * BH;
+  const long long blocks = num_ctas(a.B, a.H, a.N);
   if (blocks > 0x7fffffffLL) {
     attn_set_error("attn_fwd: too many query blocks (%lld)", blocks);
     return cudaErrorInvalidValue;
   }
+  const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mo;
   CUresult r = make_map_3d(&mq, a.q, a.D, a.N, BH);
   if (r == CUDA_SUCCESS) r = make_map_3d(&mk, a.k, a.D, a.N, BH);

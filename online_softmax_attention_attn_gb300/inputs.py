@@ -66,6 +66,8 @@ FP32_PAGE2_CAUSAL = MHAConfig("fp32 MHA causal B4 H8 N8192 D64", 4, 8, 8192,
                               64, True, torch.float32, 1002)
 BF16_PREFILL = MHAConfig("bf16 MHA causal prefill B4 H16 N4096 D128", 4, 16,
                          4096, 128, True, torch.bfloat16, 1003)
+BF16_PREFILL_NONCAUSAL = MHAConfig("bf16 MHA prefill B4 H16 N4096 D128", 4, 16, 4096,
+                                   128, False, torch.bfloat16, 1003)
 MLA_B64 = MLAConfig("bf16 MLA decode batch64 Hq128 seq4096", 64, 128, 4096,
                     4096, False, 1004)
 MLA_B256_PAGED = MLAConfig("bf16 MLA decode batch256 Hq128 seq1024-4096 paged",
