@@ -17,17 +17,21 @@
 //     OF TWO CTAs shares each work item by columns: rank 0 owns latent
 //     columns [0,256) plus the 64 RoPE columns, rank 1 owns [256,512).  Each
 //     CTA TMA-loads only its own columns of every cached row (HBM is read
-//     once), computes a partial S over them, and the two partial S tiles are
-//     swapped through distributed shared memory so that both hold the full S
-//     and run the identical softmax.  Each then accumulates its 256 columns
-//     of O = P V in TMEM (V is the same shared-memory bytes as K).
-//   * Pages of 64 tokens are consumed as two 32-token steps; the block table
-//     is read on the device and bounds-checked; K/V stream through a
-//     5-stage mbarrier ring filled by one producer warp.
-//   * Work is the flat list of all sequences' pages cut into equal chunks,
-//     one chunk per cluster (persistent).  A sequence cut by a chunk edge
-//     writes fp32 partials (O_s normalised, LSE_s) that a small combine
-//     kernel merges; sequences inside one chunk write bf16 O directly.
+//     once) and computes a partial S over them with its share of q held in
+//     TMEM.  The partial S tiles are pushed into the peer's shared memory with
+//     st.async (arrival counted in bytes on the peer's mbarrier, so no thread
+//     issues a cluster-scope fence), both CTAs add them in the same order and
+//     run the identical softmax, and each accumulates its 256 columns of
+//     O = P V in TMEM (V is the same shared-memory bytes as K).
+//   * Pages of 64 tokens are consumed as two 32-token steps through a 7-stage
+//     TMA ring; the block table is read on the device and bounds-checked.
+//     Three S buffers let the tensor core run up to three steps ahead of the
+//     softmax, and the softmax sends step i+1 before finishing step i.
+//   * Work is a list of page ranges ("chunks") of the flat page order, one
+//     chunk per cluster at a time (persistent).  The device planner either
+//     gives each sequence its own chunk (no partials) or cuts the flat order
+//     into equal chunks, moving cuts to nearby sequence starts; a sequence cut
+//     by a chunk edge writes fp32 partials that a small combine kernel merges.
 //   * Every wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
 #include <math.h>
 
@@ -46,65 +50,82 @@ constexpr int kPage = 64;
 constexpr int kStep = 32;                 // tokens per pipeline step (half page)
 constexpr int kThreads = 192;             // 4 softmax warps + producer + MMA
 constexpr int kMaxAtoms = 5;              // 64-column atoms per CTA (rank 0)
-constexpr int kQAtomBytes = kHq * 128;    // 128 heads x 64 bf16
 constexpr int kKAtomBytes = kStep * 128;  // 32 tokens x 64 bf16
 constexpr int kStageBytes = kMaxAtoms * kKAtomBytes;  // 20 KB
-constexpr int kStages = 5;
-constexpr int kXRow = 36;                 // floats per exchange row (32 + pad)
+constexpr int kStages = 7;
+constexpr int kSBufs = 3;                 // TMEM S buffers
+constexpr int kXBufs = 4;                 // partial-S receive buffers
+constexpr int kXRow = 36;                 // floats per receive row (32 + pad)
 constexpr int kXBufBytes = kHq * kXRow * 4;
+constexpr uint32_t kXBytes = kHq * kStep * 4;  // payload per step
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kQOff = 0;
-constexpr int kStageOff = kQOff + kMaxAtoms * kQAtomBytes;     // 80 KB
-constexpr int kXOff = kStageOff + kStages * kStageBytes;        // +100 KB
-constexpr int kBarOff = kXOff + 2 * kXBufBytes;                 // +36 KB
-// barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], xfull[2],
-// xfree[2], p_full[2], pv_done, o_free, mma_drain
-constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 2 + 3;
+constexpr int kStageOff = 0;
+constexpr int kXOff = kStageOff + kStages * kStageBytes;
+constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
+// barriers: kv_full[S], kv_empty[S], s_full[3], p_full[3], xfull[4], q_full,
+// q_free, pv_done, o_free, mma_drain, o_ready
+constexpr int kNumBars = 2 * kStages + 2 * kSBufs + kXBufs + 6;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
-constexpr uint32_t kColS = 256;   // 2 x 32 columns
+constexpr uint32_t kColQ = 256;   // up to 160 columns (5 atoms x 32)
+constexpr uint32_t kColS = 416;   // 3 x 32 columns
 
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
-  size_t header, prefix, plse, po, total;
-  int max_slots;
+  size_t header, prefix, bounds, plse, po, total;
+  int max_chunks;
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ constexpr WsLayout ws_layout(int B, int max_slots) {
+__host__ __device__ constexpr WsLayout ws_layout(int B, int max_chunks) {
   WsLayout w{};
-  w.max_slots = max_slots;
+  w.max_chunks = max_chunks;
   w.header = 0;
   w.prefix = 64;
-  w.plse = align_up(w.prefix + sizeof(int) * (size_t)(B + 1), 256);
-  w.po = align_up(w.plse + sizeof(float) * (size_t)max_slots * kHq, 256);
-  w.total = align_up(w.po + sizeof(float) * (size_t)max_slots * kHq * kDv, 256);
+  w.bounds = align_up(w.prefix + sizeof(int) * (size_t)(B + 1), 16);
+  w.plse = align_up(w.bounds + sizeof(int) * (size_t)(max_chunks + 1), 256);
+  w.po = align_up(w.plse + sizeof(float) * (size_t)(2 * max_chunks) * kHq, 256);
+  w.total = align_up(w.po + sizeof(float) * (size_t)(2 * max_chunks) * kHq * kDv, 256);
   return w;
 }
 
 inline int max_chunks_for(int B, int max_blocks, int num_sms, int pps) {
-  const int clusters = num_sms / 2;
   if (pps > 0) {
     const long long total = (long long)B * max_blocks;
     return (int)((total + pps - 1) / pps);
   }
-  return clusters;
+  return num_sms / 2;  // per-sequence chunks only when B <= clusters
+}
+
+__device__ __forceinline__ int find_range(const int* __restrict__ edges, int n, int x) {
+  // largest i in [0, n) with edges[i] <= x < edges[i+1] (edges non-decreasing)
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (edges[mid + 1] <= x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
 }
 
 // ---- plan -------------------------------------------------------------------
-// One CTA: validates lengths, writes the exclusive page prefix, the chunk
-// length (pages per split) and the chunk count into the workspace header.
+// One CTA.  Validates lengths, writes the exclusive page prefix, then the
+// chunk edges: per-sequence chunks when that is cheaper (no partials), else
+// ceil(T / clusters) pages per chunk with each cut moved to a sequence start
+// within 1/8 chunk, or a fixed split length when one is forced.
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restrict__ seqlens,
                                                         int B, int max_blocks, int clusters,
-                                                        int pps_override, int* __restrict__ ws_hdr,
-                                                        int* __restrict__ prefix, int* err) {
+                                                        int pps_override, int* __restrict__ hdr,
+                                                        int* __restrict__ prefix,
+                                                        int* __restrict__ bounds, int* err) {
   __shared__ int warp_sums[32];
-  __shared__ int carry;
-  if (threadIdx.x == 0) carry = 0;
+  __shared__ int warp_max[32];
+  __shared__ int carry, maxn_s, nchunks_s, pps_s, mode_s;
+  if (threadIdx.x == 0) { carry = 0; maxn_s = 0; }
   __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -112,29 +133,30 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     int n = 0;
     if (b < B) {
       const int L = seqlens[b];
-      if (L < 0 || L > max_blocks * kPage) {
-        record_error(err, ATTN_ERR_BAD_SEQLEN, 0, b);
-      } else {
-        n = (L + kPage - 1) / kPage;
-      }
+      if (L < 0 || L > max_blocks * kPage) record_error(err, ATTN_ERR_BAD_SEQLEN, 0, b);
+      else n = (L + kPage - 1) / kPage;
     }
-    // inclusive scan within the warp, then across warps
-    int x = n;
+    int x = n, mx = n;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, x, off);
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
       if (lane >= off) x += y;
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
     if (lane == 31) warp_sums[wid] = x;
+    if (lane == 0) warp_max[wid] = mx;
     __syncthreads();
     if (wid == 0) {
-      int w = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+      int w = warp_sums[lane];
+      int m = warp_max[lane];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, w, off);
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
         if (lane >= off) w += y;
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
       }
       warp_sums[lane] = w;
+      if (lane == 0) maxn_s = max(maxn_s, m);
     }
     __syncthreads();
     const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
@@ -146,11 +168,56 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   if (threadIdx.x == 0) {
     const int T = carry;
     prefix[B] = T;
-    int pps = pps_override > 0 ? pps_override : (T + clusters - 1) / max(clusters, 1);
-    if (pps < 1) pps = 1;
-    ws_hdr[0] = T;
-    ws_hdr[1] = pps;
-    ws_hdr[2] = (T + pps - 1) / pps;
+    int mode, pps, nchunks;
+    if (pps_override > 0) {
+      mode = 0;
+      pps = pps_override;
+      nchunks = (T + pps - 1) / pps;
+    } else {
+      pps = max(1, (T + clusters - 1) / max(clusters, 1));
+      // time model: per-cluster pages (tensor-bound) vs bytes (HBM-bound),
+      // split partials cost 2 x 256 KB of traffic each
+      const float page_us = 0.65f, bytes_per_us = 6.5e6f;
+      const float kv = (float)T * kPage * 1152.f;
+      const int n_a = (T + pps - 1) / pps;
+      const float est_a = fmaxf(pps * page_us, (kv + 2.f * n_a * 2.f * 262144.f) / bytes_per_us);
+      const float est_b = fmaxf(maxn_s * page_us, kv / bytes_per_us);
+      if (B <= clusters && est_b <= est_a) {
+        mode = 1;
+        nchunks = B;
+      } else {
+        mode = 2;
+        nchunks = n_a;
+      }
+    }
+    mode_s = mode;
+    pps_s = pps;
+    nchunks_s = nchunks;
+    hdr[0] = T;
+    hdr[1] = nchunks;
+    hdr[2] = pps;
+    hdr[3] = mode;
+  }
+  __syncthreads();
+  const int T = carry, mode = mode_s, pps = pps_s, nchunks = nchunks_s;
+  for (int k = threadIdx.x; k <= nchunks; k += blockDim.x) {
+    int x;
+    if (mode == 1) {
+      x = prefix[k];
+    } else {
+      x = min(k * pps, T);
+      if (mode == 2 && k > 0 && k < nchunks) {
+        const int b = find_range(prefix, B, x);
+        const int s0 = prefix[b], s1 = prefix[b + 1];
+        const int tol = pps / 8;
+        if (x - s0 <= s1 - x) {
+          if (x - s0 <= tol) x = s0;
+        } else if (s1 - x <= tol) {
+          x = s1;
+        }
+      }
+    }
+    bounds[k] = x;
   }
 }
 
@@ -160,26 +227,16 @@ struct Seg {
   int slot;       // partial slot, or -1 when the segment is the whole sequence
 };
 
-__device__ __forceinline__ int find_batch(const int* __restrict__ prefix, int B, int page) {
-  // largest b with prefix[b] <= page < prefix[b+1]
-  int lo = 0, hi = B;  // search in prefix[0..B]
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (prefix[mid + 1] <= page) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// Enumerates the segments of chunk k in order; returns false when done.
+// Enumerates the sequence segments of chunk k in order.
 struct ChunkIter {
   const int* prefix;
-  int B, k, pps, start, end, b;
-  __device__ void init(const int* pf, int B_, int k_, int pps_, int T) {
-    prefix = pf; B = B_; k = k_; pps = pps_;
-    start = k * pps;
-    end = min(start + pps, T);
-    b = (start < end) ? find_batch(prefix, B, start) : B;
+  int B, k, start, end, first_page, b;
+  __device__ void init(const int* pf, const int* bounds, int B_, int k_) {
+    prefix = pf; B = B_; k = k_;
+    start = bounds[k];
+    end = bounds[k + 1];
+    first_page = start;
+    b = (start < end) ? find_range(prefix, B, start) : B;
   }
   __device__ bool next(Seg& s) {
     if (start >= end || b >= B) return false;
@@ -189,7 +246,7 @@ struct ChunkIter {
     s.p1 = seg_end - prefix[b];
     const int npages = prefix[b + 1] - prefix[b];
     const bool whole = (s.p0 == 0 && s.p1 == npages);
-    const bool first = (start == k * pps);
+    const bool first = (start == first_page);
     s.slot = whole ? -1 : (first ? 2 * k : 2 * k + 1);
     start = seg_end;
     ++b;
@@ -198,15 +255,20 @@ struct ChunkIter {
   }
 };
 
+__device__ __forceinline__ int seg_steps(int p0, int p1, int L) {
+  const int t0 = p0 * kPage, t_end = min(p1 * kPage, L);
+  return (t_end - t0 + kStep - 1) / kStep;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmKV,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV,
+                      const __nv_bfloat16* __restrict__ q,
                       const int32_t* __restrict__ block_table,
                       const int32_t* __restrict__ seqlens, __nv_bfloat16* __restrict__ o,
-                      float* __restrict__ lse, const int* __restrict__ ws_hdr,
-                      const int* __restrict__ prefix, float* __restrict__ part_lse,
-                      float* __restrict__ part_o, int B, int max_blocks, int num_blocks,
-                      float scale_log2, int* err) {
+                      float* __restrict__ lse, const int* __restrict__ hdr,
+                      const int* __restrict__ prefix, const int* __restrict__ bounds,
+                      float* __restrict__ part_lse, float* __restrict__ part_o, int B,
+                      int max_blocks, int num_blocks, float scale_log2, int* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -216,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
-  const int T = ws_hdr[0], pps = ws_hdr[1], nchunks = ws_hdr[2];
+  const int nchunks = hdr[1];
   if (cluster >= nchunks) return;  // both CTAs of the cluster leave together
 
   // columns owned by this CTA, as 64-column atoms of the 576-wide row
@@ -225,44 +287,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return rank == 0 ? (a < 4 ? a * 64 : 512) : (256 + a * 64);
   };
 
-  const uint32_t sQ = base + kQOff;
   const uint32_t sStage = base + kStageOff;
   const uint32_t sX = base + kXOff;
   const uint32_t bar0 = base + kBarOff;
-  const uint32_t bar_q_full = bar0, bar_q_empty = bar0 + 8;
-  auto bar_kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (2 + kStages + s); };
-  auto bar_s_full = [&](int b) { return bar0 + 8u * (2 + 2 * kStages + b); };
-  auto bar_xfull = [&](int b) { return bar0 + 8u * (4 + 2 * kStages + b); };
-  auto bar_xfree = [&](int b) { return bar0 + 8u * (6 + 2 * kStages + b); };
-  auto bar_p_full = [&](int b) { return bar0 + 8u * (8 + 2 * kStages + b); };
-  const uint32_t bar_pv_done = bar0 + 8u * (10 + 2 * kStages);
-  const uint32_t bar_o_free = bar0 + 8u * (11 + 2 * kStages);
-  const uint32_t bar_mma_drain = bar0 + 8u * (12 + 2 * kStages);
+  auto bar_kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto bar_s_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (2 * kStages + kSBufs + b); };
+  auto bar_xfull = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kSBufs + b); };
+  const uint32_t bar_q_full = bar0 + 8u * (2 * kStages + 2 * kSBufs + kXBufs);
+  const uint32_t bar_q_free = bar_q_full + 8;
+  const uint32_t bar_pv_done = bar_q_full + 16;
+  const uint32_t bar_o_free = bar_q_full + 24;
+  const uint32_t bar_mma_drain = bar_q_full + 32;
+  // o_ready completes once per segment, after that segment's last PV: the
+  // epilogue waits on it (pv_done completes once per step and may lag by more
+  // than one phase at that point, so its parity would be ambiguous there).
+  const uint32_t bar_o_ready = bar_q_full + 40;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar_s_full(b), 1);
-      mbar_init(bar_xfull(b), 128);
-      mbar_init(bar_xfree(b), 128);
       mbar_init(bar_p_full(b), 128);
     }
+    for (int b = 0; b < kXBufs; ++b) mbar_init(bar_xfull(b), 1);
+    mbar_init(bar_q_full, 128);
+    mbar_init(bar_q_free, 1);
     mbar_init(bar_pv_done, 1);
     mbar_init(bar_o_free, 128);
     mbar_init(bar_mma_drain, 1);
+    mbar_init(bar_o_ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmQ);
+    // arm the receive barriers for steps 0..3 (re-armed after each use)
+    for (int b = 0; b < kXBufs; ++b) mbar_arrive_expect_tx(bar_xfull(b), kXBytes);
     prefetch_tmap(&tmKV);
   }
   if (warp == 5) {
@@ -271,32 +337,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peer barriers are initialised before any remote arrive
+  cluster_sync();  // the peer's barriers are initialised before any remote store
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 4) {
-    // ================= producer =================
+    // ================= producer: paged K/V (own columns) =================
     if (lane == 0) {
       const uint64_t pol_kv = policy_evict_first();  // every cached row is read once
-      int g = 0, seg_i = 0;
-      int issued = 0;  // steps [0, issued) have their loads issued
+      int g = 0, issued = 0;
       bool ok = true;
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, B, k, pps, T);
+        it.init(prefix, bounds, B, k);
         Seg s;
         while (ok && it.next(s)) {
-          if (seg_i > 0) {
-            ok = mbar_wait(bar_q_empty, (seg_i - 1) & 1, abort_flag, err, kSiteQFull, seg_i);
-            if (!ok) break;
-          }
-          mbar_arrive_expect_tx(bar_q_full, natoms * kQAtomBytes);
-          for (int a = 0; a < natoms; ++a)
-            tma_load_2d(sQ + a * kQAtomBytes, &tmQ, bar_q_full, atom_col(a), s.b * kHq);
           const int L = seqlens[s.b];
           const int t_end = min(s.p1 * kPage, L);
-          for (int t = s.p0 * kPage; t < t_end && ok; t += kStep, ++g) {
+          for (int t = s.p0 * kPage; t < t_end; t += kStep, ++g) {
             const int slot = g % kStages, use = g / kStages;
             if (use > 0) {
               ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
@@ -315,7 +373,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                pol_kv);
             issued = g + 1;
           }
-          ++seg_i;
         }
       }
       if (!ok) {
@@ -323,10 +380,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int gg = first; gg < issued; ++gg) {
           volatile int never = 0;
           mbar_wait(bar_kv_full(gg % kStages), (gg / kStages) & 1, &never, nullptr, kSiteDrain, gg);
-        }
-        if (seg_i > 0) {
-          volatile int never = 0;
-          mbar_wait(bar_q_full, (seg_i - 1) & 1, &never, nullptr, kSiteDrain, -1);
         }
       }
     }
@@ -337,66 +390,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = idesc_bf16(kHq, kStep, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kHq, 256, false, true);
       const uint32_t tO = tbase + kColO;
-      const uint32_t tS = tbase + kColS;
+      const uint32_t tQ = tbase + kColQ;
       int g = 0, seg_i = 0;
       bool ok = true;
-      // S for global step gs of the current segment (Q resident)
-      auto issue_s = [&](int gs) -> bool {
-        const int slot = gs % kStages;
-        if (!mbar_wait(bar_kv_full(slot), (gs / kStages) & 1, abort_flag, err, kSiteKvFull, gs))
+      // S partial for global step gg: A = this CTA's q columns (TMEM), B = K atoms.
+      auto issue_s = [&](int gg) -> bool {
+        const int slot = gg % kStages;
+        if (!mbar_wait(bar_kv_full(slot), (gg / kStages) & 1, abort_flag, err, kSiteKvFull, gg))
           return false;
         tc_fence_after();
         const uint32_t kb = sStage + slot * kStageBytes;
+        const uint32_t tS = tbase + kColS + (gg % kSBufs) * 32;
         for (int a = 0; a < natoms; ++a) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ss(tS + (gs & 1) * 32, sdesc_sw128(sQ + a * kQAtomBytes + kk * 32, 16, 1024),
-                   sdesc_sw128(kb + a * kKAtomBytes + kk * 32, 16, 1024), kIdescS,
-                   (a | kk) != 0);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tS, tQ + a * 32 + kk * 8, sdesc_sw128(kb + a * kKAtomBytes + kk * 32, 16, 1024),
+                   kIdescS, (a | kk) != 0);
         }
-        tc_commit(bar_s_full(gs & 1));
+        tc_commit(bar_s_full(gg % kSBufs));
         return true;
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, B, k, pps, T);
+        it.init(prefix, bounds, B, k);
         Seg s;
         while (ok && it.next(s)) {
-          const int L = seqlens[s.b];
-          const int t0 = s.p0 * kPage, t_end = min(s.p1 * kPage, L);
-          const int nsteps = (t_end - t0 + kStep - 1) / kStep;
+          const int n = seg_steps(s.p0, s.p1, seqlens[s.b]);
           ok = mbar_wait(bar_q_full, seg_i & 1, abort_flag, err, kSiteQFull, seg_i);
           if (!ok) break;
           tc_fence_after();
-          if (nsteps > 0) ok = issue_s(g);
-          if (ok && nsteps > 1) ok = issue_s(g + 1);
-          if (ok && nsteps <= 2) tc_commit(bar_q_empty);  // all S of this segment issued
+          for (int i = 0; i < n && i < kSBufs && ok; ++i) ok = issue_s(g + i);
+          if (ok && n <= kSBufs) tc_commit(bar_q_free);  // every S of this segment issued
           if (ok && seg_i > 0) {
             ok = mbar_wait(bar_o_free, (seg_i - 1) & 1, abort_flag, err, kSitePvDone, seg_i);
             tc_fence_after();
           }
-          for (int i = 0; i < nsteps && ok; ++i) {
+          for (int i = 0; i < n && ok; ++i) {
             const int gi = g + i;
-            ok = mbar_wait(bar_p_full(gi & 1), (gi >> 1) & 1, abort_flag, err, kSitePFull, gi);
+            ok = mbar_wait(bar_p_full(gi % kSBufs), (gi / kSBufs) & 1, abort_flag, err, kSitePFull, gi);
             if (!ok) break;
             tc_fence_after();
             const int slot = gi % kStages;
             const uint32_t vb = sStage + slot * kStageBytes;
 #pragma unroll
-            for (int kk = 0; kk < kStep / 16; ++kk) {
-              mma_ts(tO, tS + (gi & 1) * 32 + kk * 8,
+            for (int kk = 0; kk < kStep / 16; ++kk)
+              mma_ts(tO, tbase + kColS + (gi % kSBufs) * 32 + kk * 8,
                      sdesc_sw128(vb + kk * 16 * 128, kKAtomBytes, 1024), kIdescPV,
                      (i > 0 || kk > 0) ? 1u : 0u);
-            }
             tc_commit(bar_kv_empty(slot));
             tc_commit(bar_pv_done);
-            if (i + 2 < nsteps) {
-              ok = issue_s(gi + 2);
-              if (ok && i + 3 == nsteps) tc_commit(bar_q_empty);
+            if (i == n - 1) tc_commit(bar_o_ready);
+            if (i + kSBufs < n) {
+              ok = issue_s(gi + kSBufs);
+              if (ok && i + kSBufs == n - 1) tc_commit(bar_q_free);
             }
           }
-          g += nsteps;
+          g += n;
           ++seg_i;
         }
       }
@@ -410,64 +459,150 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;  // head == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tbase + lane_off + kColO;
-    const uint32_t tS = tbase + lane_off + kColS;
-    const uint32_t my_x = sX + r * kXRow * 4;
-    const uint32_t peer_x = mapa_shared(my_x, peer);
+    const uint32_t tQ = tbase + lane_off + kColQ;
+    const uint32_t tS0 = tbase + lane_off + kColS;
+    const uint32_t peer_row = mapa_shared(sX + r * kXRow * 4, peer);
+    const uint32_t peer_xfull0 = mapa_shared(bar_xfull(0), peer);
+    const float* my_row = reinterpret_cast<const float*>(smem + kXOff + r * kXRow * 4);
+    constexpr float kLn2 = 0.69314718055994530942f;
     int g = 0, seg_i = 0;
     bool ok = true;
+    // the previous segment, whose epilogue runs once the next q is in place
+    int prev_b = -1, prev_slot = -1, prev_seg = 0;
+    float prev_m = 0.f, prev_l = 0.f;
+
+    // A(gg): own partial S of step gg -> registers, and pushed to the peer.
+    auto stepA = [&](int gg, float* sv) -> bool {
+      const int sb = gg % kSBufs;
+      bool w = mbar_wait(bar_s_full(sb), (gg / kSBufs) & 1, abort_flag, err, kSiteSFull, gg);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) return false;
+      tc_fence_after();
+      tmem_ld32(tS0 + sb * 32, sv);
+      const int xb = gg % kXBufs;
+      const uint32_t dst = peer_row + xb * kXBufBytes;
+      const uint32_t rbar = peer_xfull0 + 8u * xb;
+#pragma unroll
+      for (int c = 0; c < kStep; c += 4)
+        st_async_v4(dst + c * 4, __float_as_uint(sv[c]), __float_as_uint(sv[c + 1]),
+                    __float_as_uint(sv[c + 2]), __float_as_uint(sv[c + 3]), rbar);
+      return true;
+    };
+
+    auto epilogue = [&]() {
+      // O / l -> bf16 (whole sequence) or fp32 partial; LSE from rank 0
+      const float inv_l = (prev_l > 0.f) ? 1.0f / prev_l : 0.f;
+      const float lse_v = (prev_l > 0.f) ? (prev_m + log2f(prev_l)) * kLn2 : -INFINITY;
+      const size_t orow = (size_t)prev_b * kHq + r;
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 32) {
+        float ov[32];
+        tmem_ld32(tO + c, ov);
+        if (prev_slot < 0) {
+          __nv_bfloat16* dst = o + orow * kDv + rank * 256 + c;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
+            w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
+            w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
+            w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
+            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
+          }
+        } else {
+          float* dst = part_o + ((size_t)prev_slot * kHq + r) * kDv + rank * 256 + c;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4*>(dst + q4 * 4) =
+                make_float4(ov[q4 * 4] * inv_l, ov[q4 * 4 + 1] * inv_l, ov[q4 * 4 + 2] * inv_l,
+                            ov[q4 * 4 + 3] * inv_l);
+        }
+      }
+      if (rank == 0) {
+        if (prev_slot < 0) lse[orow] = lse_v;
+        else part_lse[(size_t)prev_slot * kHq + r] = lse_v;
+      }
+      tc_fence_before();
+      mbar_arrive(bar_o_free);
+    };
+
     for (int k = cluster; k < nchunks && ok; k += nclusters) {
       ChunkIter it;
-      it.init(prefix, B, k, pps, T);
+      it.init(prefix, bounds, B, k);
       Seg s;
       while (ok && it.next(s)) {
         const int L = seqlens[s.b];
-        const int t0 = s.p0 * kPage, t_end = min(s.p1 * kPage, L);
-        const int nsteps = (t_end - t0 + kStep - 1) / kStep;
-        float m_ref = -INFINITY, l = 0.f;
-        for (int i = 0; i < nsteps && ok; ++i) {
-          const int gi = g + i, buf = gi & 1, use = gi >> 1;
-          ok = mbar_wait(bar_s_full(buf), use & 1, abort_flag, err, kSiteSFull, gi);
+        const int t0 = s.p0 * kPage;
+        const int n = seg_steps(s.p0, s.p1, L);
+        // ---- this segment's q columns -> TMEM (A operand of the S MMAs)
+        if (seg_i > 0) {
+          ok = mbar_wait(bar_q_free, (seg_i - 1) & 1, abort_flag, err, kSiteQFull, seg_i);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        {
+          const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + r) * kDk);
+          for (int a = 0; a < natoms; ++a) {
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = __ldg(qrow + atom_col(a) / 8 + c);
+              w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+            }
+            tmem_st32(tQ + a * 32, w);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_q_full);
+        }
+        // ---- the previous segment's epilogue overlaps this segment's first S
+        if (prev_b >= 0) {
+          ok = mbar_wait(bar_o_ready, prev_seg & 1, abort_flag, err, kSitePvDone, prev_seg);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
-          float sv[kStep];
-          tmem_ld32(tS + buf * 32, sv);
-          // ---- swap partial S with the peer CTA through DSMEM
-          if (use > 0) {
-            ok = mbar_wait<true>(bar_xfree(buf), (use - 1) & 1, abort_flag, err, kSiteXfree, gi);
-            ok = __all_sync(0xffffffffu, ok);
+          epilogue();
+          prev_b = -1;
+        }
+        // ---- steps: send step i+1 before finishing step i
+        float m_ref = -INFINITY, l = 0.f;
+        float scur[kStep];
+        ok = stepA(g, scur);
+        for (int i = 0; i < n && ok; ++i) {
+          const int gi = g + i;
+          float snext[kStep];
+          if (i + 1 < n) {
+            ok = stepA(gi + 1, snext);
             if (!ok) break;
           }
-          const uint32_t dst = peer_x + buf * kXBufBytes;
-#pragma unroll
-          for (int c = 0; c < kStep; c += 4) st_cluster_v4(dst + c * 4, sv[c], sv[c + 1], sv[c + 2], sv[c + 3]);
-          mbar_arrive_cluster(bar_xfull(buf), peer);
-          ok = mbar_wait<true>(bar_xfull(buf), use & 1, abort_flag, err, kSiteXchg, gi);
+          // peer's partial of step gi -> full S (same sum order on both CTAs)
+          const int xb = gi % kXBufs;
+          ok = mbar_wait<true>(bar_xfull(xb), (gi / kXBufs) & 1, abort_flag, err, kSiteXchg, gi);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          const float* xin = reinterpret_cast<const float*>(smem + kXOff + buf * kXBufBytes +
-                                                            r * kXRow * 4);
+          const float* xin = my_row + xb * (kXBufBytes / 4);
 #pragma unroll
           for (int c = 0; c < kStep; c += 4) {
             const float4 pv = *reinterpret_cast<const float4*>(xin + c);
-            // identical sum order on both CTAs: rank-0 partial + rank-1 partial
             if (rank == 0) {
-              sv[c] += pv.x; sv[c + 1] += pv.y; sv[c + 2] += pv.z; sv[c + 3] += pv.w;
+              scur[c] += pv.x; scur[c + 1] += pv.y; scur[c + 2] += pv.z; scur[c + 3] += pv.w;
             } else {
-              sv[c] = pv.x + sv[c]; sv[c + 1] = pv.y + sv[c + 1];
-              sv[c + 2] = pv.z + sv[c + 2]; sv[c + 3] = pv.w + sv[c + 3];
+              scur[c] = pv.x + scur[c]; scur[c + 1] = pv.y + scur[c + 1];
+              scur[c + 2] = pv.z + scur[c + 2]; scur[c + 3] = pv.w + scur[c + 3];
             }
           }
-          mbar_arrive_cluster(bar_xfree(buf), peer);
+          // Re-arm this receive buffer for step gi + 4.  The peer can only
+          // send that step after this CTA has sent step gi + 2, which every
+          // thread does after this read.
+          if (r == 0) mbar_arrive_expect_tx(bar_xfull(xb), kXBytes);
 
           // ---- mask tokens at or past the sequence end, online softmax
-          const int tok0 = t0 + i * kStep;
-          const int nvalid = L - tok0;
+          const int nvalid = L - (t0 + i * kStep);
           float mt = -INFINITY;
 #pragma unroll
           for (int c = 0; c < kStep; ++c) {
-            sv[c] = (c < nvalid) ? sv[c] * scale_log2 : -INFINITY;
-            mt = fmaxf(mt, sv[c]);
+            scur[c] = (c < nvalid) ? scur[c] * scale_log2 : -INFINITY;
+            mt = fmaxf(mt, scur[c]);
           }
           const float m_new = fmaxf(m_ref, mt);
           const bool resc = m_new > m_ref + kRescaleThreshold;
@@ -479,18 +614,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           uint32_t p[kStep / 2];
-          float rs = 0.f;
+          float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
           for (int c = 0; c < kStep; c += 2) {
-            const float p0 = fast_exp2(sv[c] - m_use);
-            const float p1 = fast_exp2(sv[c + 1] - m_use);
-            rs += p0 + p1;
+            const float p0 = fast_exp2(scur[c] - m_use);
+            const float p1 = fast_exp2(scur[c + 1] - m_use);
+            rs0 += p0;
+            rs1 += p1;
             p[c / 2] = pack_bf16x2(p0, p1);
           }
-          l += rs;
-          tmem_st16(tS + buf * 32, p);
+          l += rs0 + rs1;
+          tmem_st16(tS0 + (gi % kSBufs) * 32, p);
           // Tokens past the end contribute exactly zero even if the cache
           // tail holds non-finite bytes: clear those V rows before PV reads.
+          // Each thread fences its own writes; the PV MMA is issued only after
+          // all 128 threads have arrived on p_full below.
           if (nvalid < kStep) {
             uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
             const int zrows = kStep - nvalid;  // rows [nvalid, 32) of atoms 0..3
@@ -501,7 +639,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
-            named_barrier_sync(1, 128);
           }
           if (i > 0 && __any_sync(0xffffffffu, resc)) {
             ok = mbar_wait(bar_pv_done, (gi - 1) & 1, abort_flag, err, kSitePvDone, gi);
@@ -514,64 +651,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tmem_ld32(tO + c, ov);
               uint32_t ou[32];
 #pragma unroll
-              for (int t = 0; t < 32; ++t) ou[t] = __float_as_uint(ov[t] * alpha);
+              for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
               tmem_st32(tO + c, ou);
             }
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(bar_p_full(buf));
+          mbar_arrive(bar_p_full(gi % kSBufs));
+#pragma unroll
+          for (int c = 0; c < kStep; ++c) scur[c] = snext[c];
         }
         if (!ok) break;
-        // ---- segment epilogue
-        const int glast = g + nsteps - 1;
-        if (nsteps > 0) {
-          ok = mbar_wait(bar_pv_done, glast & 1, abort_flag, err, kSitePvDone, glast);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
-        constexpr float kLn2 = 0.69314718055994530942f;
-        const float lse_v = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-        const size_t orow = (size_t)s.b * kHq + r;
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float ov[32];
-          if (nsteps > 0) {
-            tmem_ld32(tO + c, ov);
-          } else {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) ov[t] = 0.f;
-          }
-          if (s.slot < 0) {
-            __nv_bfloat16* dst = o + orow * kDv + rank * 256 + c;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
-              w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
-              w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
-              w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
-              *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
-            }
-          } else {
-            float* dst = part_o + ((size_t)s.slot * kHq + r) * kDv + rank * 256 + c;
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              *reinterpret_cast<float4*>(dst + q4 * 4) =
-                  make_float4(ov[q4 * 4] * inv_l, ov[q4 * 4 + 1] * inv_l,
-                              ov[q4 * 4 + 2] * inv_l, ov[q4 * 4 + 3] * inv_l);
-          }
-        }
-        if (rank == 0) {
-          if (s.slot < 0) lse[orow] = lse_v;
-          else part_lse[(size_t)s.slot * kHq + r] = lse_v;
-        }
-        tc_fence_before();
-        mbar_arrive(bar_o_free);
-        g += nsteps;
+        prev_b = s.b;
+        prev_slot = s.slot;
+        prev_seg = seg_i;
+        prev_m = m_ref;
+        prev_l = l;
+        g += n;
         ++seg_i;
+      }
+    }
+    if (ok && prev_b >= 0) {
+      ok = mbar_wait(bar_o_ready, prev_seg & 1, abort_flag, err, kSitePvDone, prev_seg);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        epilogue();
       }
     }
   }
@@ -590,13 +695,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // by the decode kernel; empty sequences get O = 0, LSE = -inf; the rest merge
 // their partials: L = log sum_s e^{L_s}, O = sum_s e^{L_s - L} O_s.
 __global__ void __launch_bounds__(256) mla_combine_kernel(
-    const int* __restrict__ ws_hdr, const int* __restrict__ prefix,
+    const int* __restrict__ hdr, const int* __restrict__ prefix, const int* __restrict__ bounds,
     const float* __restrict__ part_lse, const float* __restrict__ part_o,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   const int b = blockIdx.x;
   const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
   const int c0 = (threadIdx.x & 15) * 32;
-  const int pps = ws_hdr[1];
+  const int nchunks = hdr[1];
   const int pb = prefix[b], pe = prefix[b + 1];
   const size_t orow = (size_t)b * kHq + h;
   if (pe == pb) {
@@ -605,19 +710,22 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
     if (c0 == 0) lse[orow] = -INFINITY;
     return;
   }
-  const int k0 = pb / pps, k1 = (pe - 1) / pps;
+  const int k0 = find_range(bounds, nchunks, pb);
+  const int k1 = find_range(bounds, nchunks, pe - 1);
   if (k0 == k1) return;  // written directly by the decode kernel
+  auto slot_of = [&](int k) { return (k == k0 && bounds[k0] != pb) ? 2 * k + 1 : 2 * k; };
   float mx = -INFINITY;
   for (int k = k0; k <= k1; ++k) {
-    const int slot = (k == k0 && pb != k0 * pps) ? 2 * k + 1 : 2 * k;
-    mx = fmaxf(mx, part_lse[(size_t)slot * kHq + h]);
+    if (bounds[k] == bounds[k + 1]) continue;
+    mx = fmaxf(mx, part_lse[(size_t)slot_of(k) * kHq + h]);
   }
   float acc[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) acc[c] = 0.f;
   float wsum = 0.f;
   for (int k = k0; k <= k1; ++k) {
-    const int slot = (k == k0 && pb != k0 * pps) ? 2 * k + 1 : 2 * k;
+    if (bounds[k] == bounds[k + 1]) continue;
+    const int slot = slot_of(k);
     const float ls = part_lse[(size_t)slot * kHq + h];
     const float w = (ls == -INFINITY) ? 0.f : expf(ls - mx);
     wsum += w;
@@ -653,48 +761,73 @@ CUresult make_map_2d(CUtensorMap* map, const void* ptr, long long rows, int box_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Clusters of two that can be resident at once (cached per device).
+int active_clusters(int num_sms) {
+  static int cached[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / 2;
+    }
+    cached[dev] = n < num_sms / 2 ? n : num_sms / 2;
+  }
+  return cached[dev];
+}
+
 }  // namespace
 
 size_t mla_workspace_bytes(int B, int Hq, int max_blocks, int num_sms, int pages_per_split) {
   (void)Hq;
-  const int chunks = max_chunks_for(B, max_blocks, num_sms, pages_per_split);
-  return ws_layout(B, 2 * chunks).total;
+  return ws_layout(B, max_chunks_for(B, max_blocks, num_sms, pages_per_split)).total;
 }
 
 cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
-  const int clusters = a.num_sms / 2;
-  const int max_chunks = max_chunks_for(a.B, a.max_blocks, a.num_sms, a.pages_per_split);
-  const WsLayout w = ws_layout(a.B, 2 * max_chunks);
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int clusters = active_clusters(a.num_sms);
+  const WsLayout w = ws_layout(a.B, max_chunks_for(a.B, a.max_blocks, a.num_sms, a.pages_per_split));
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int* hdr = reinterpret_cast<int*>(ws + w.header);
   int* prefix = reinterpret_cast<int*>(ws + w.prefix);
+  int* bounds = reinterpret_cast<int*>(ws + w.bounds);
   float* plse = reinterpret_cast<float*>(ws + w.plse);
   float* po = reinterpret_cast<float*>(ws + w.po);
 
-  CUtensorMap mq, mkv;
-  CUresult r = make_map_2d(&mq, a.q, (long long)a.B * kHq, kHq);
-  if (r == CUDA_SUCCESS) r = make_map_2d(&mkv, a.kv, (long long)a.num_blocks * kPage, kStep);
+  CUtensorMap mkv;
+  CUresult r = make_map_2d(&mkv, a.kv, (long long)a.num_blocks * kPage, kStep);
   if (r != CUDA_SUCCESS) {
     attn_set_error("mla_decode: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return cudaErrorInvalidValue;
   }
-  // With a fixed split length the chunk count may exceed the cluster count:
-  // clusters then loop over chunks.  The automatic plan makes at most one
-  // chunk per cluster.
   mla_plan_kernel<<<1, 1024, 0, s>>>(a.seqlens, a.B, a.max_blocks, clusters, a.pages_per_split,
-                                     hdr, prefix, a.err);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+                                     hdr, prefix, bounds, a.err);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   mla_decode_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(
-      mq, mkv, a.block_table, a.seqlens, static_cast<__nv_bfloat16*>(a.o), a.lse, hdr, prefix,
-      plse, po, a.B, a.max_blocks, a.num_blocks, scale_log2, a.err);
+      mkv, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
+      static_cast<__nv_bfloat16*>(a.o), a.lse, hdr, prefix, bounds, plse, po, a.B, a.max_blocks,
+      a.num_blocks, scale_log2, a.err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_combine_kernel<<<dim3(a.B, kHq / 16), 256, 0, s>>>(hdr, prefix, plse, po,
+  mla_combine_kernel<<<dim3(a.B, kHq / 16), 256, 0, s>>>(hdr, prefix, bounds, plse, po,
                                                          static_cast<__nv_bfloat16*>(a.o), a.lse);
   return cudaGetLastError();
 }
@@ -703,13 +836,13 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
 // mla_decode_noalloc runs the same plan / decode / combine kernels with the
 // workspace placed in this file-scope device array instead of a caller
 // buffer.  Its size covers the automatic plan for up to kNoAllocMaxBatch
-// sequences on a device of up to kNoAllocMaxSms SMs (2 partial slots per
-// 2-SM cluster).  Every GPU that loads the library reserves it until exit.
+// sequences on a device of up to kNoAllocMaxSms SMs (at most one chunk per
+// 2-SM cluster, two partial slots per chunk).  Every GPU that loads the
+// library reserves it until exit.
 namespace {
 constexpr int kNoAllocMaxBatch = 8192;
 constexpr int kNoAllocMaxSms = 160;
-constexpr size_t kNoAllocScratchBytes =
-    ws_layout(kNoAllocMaxBatch, 2 * (kNoAllocMaxSms / 2)).total;
+constexpr size_t kNoAllocScratchBytes = ws_layout(kNoAllocMaxBatch, kNoAllocMaxSms / 2).total;
 static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size");
 
 static __device__ __align__(256) uint8_t g_mla_noalloc_scratch[kNoAllocScratchBytes];
