@@ -285,70 +285,113 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int nvalid = lim - j * kBN;  // keys k < nvalid of this block are visible
       const bool full = nvalid >= kBN;
-      float mt;
-      if (full) {
-        // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
-        float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-        if (scale_log2 >= 0.f) {
-#pragma unroll
-          for (int c = 4; c < kBN; c += 4) {
-            a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
-            a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
-          }
-          mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
-        } else {
-#pragma unroll
-          for (int c = 4; c < kBN; c += 4) {
-            a0 = fminf(a0, s[c]); a1 = fminf(a1, s[c + 1]);
-            a2 = fminf(a2, s[c + 2]); a3 = fminf(a3, s[c + 3]);
-          }
-          mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
-        }
-      } else {
-        mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] = (c < nvalid) ? s[c] * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, s[c]);
-        }
-      }
-      const float m_new = fmaxf(m_ref, mt);
-      const bool resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
       float alpha = 1.f;
-      if (resc) {
-        alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
-        m_ref = m_new;
-        l *= alpha;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = 2^(t - m), packed to bf16 pairs and written over the S columns
-      // in two halves of 64 keys (32 TMEM columns each).
-      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+      bool resc = false;
+      // Fast path (block fully visible, reference already set, scale >= 0):
+      // P = 2^(scale*s - m_ref) is computed with the CURRENT reference while
+      // the row max is reduced alongside, so the max is off the critical
+      // path.  The result is kept unless the max grew by more than 2^8 (rare
+      // after the first block); then S is reloaded from TMEM and the block is
+      // redone on the slow path below.  Both give the same P (the row sum
+      // differs only in its rounding order).
+      bool done = false;
+      if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
+        uint32_t p[kBN / 2];
+        float a[8], rr[8];
+        const float nm = -m_ref;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t p[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const int k = h * 64 + c;
-          float p0, p1, p2, p3;
-          if (full) {
-            p0 = fast_exp2(fmaf(s[k], scale_log2, -m_use));
-            p1 = fast_exp2(fmaf(s[k + 1], scale_log2, -m_use));
-            p2 = fast_exp2(fmaf(s[k + 2], scale_log2, -m_use));
-            p3 = fast_exp2(fmaf(s[k + 3], scale_log2, -m_use));
-          } else {
-            p0 = fast_exp2(s[k] - m_use);
-            p1 = fast_exp2(s[k + 1] - m_use);
-            p2 = fast_exp2(s[k + 2] - m_use);
-            p3 = fast_exp2(s[k + 3] - m_use);
-          }
-          r0 += p0; r1 += p1; r2 += p2; r3 += p3;
-          p[c / 2] = pack_bf16x2(p0, p1);
-          p[c / 2 + 1] = pack_bf16x2(p2, p3);
+        for (int u = 0; u < 8; ++u) {
+          a[u] = s[u];
+          rr[u] = 0.f;
         }
-        tmem_st32(tS + h * 32, p);
+#pragma unroll
+        for (int c = 0; c < kBN; c += 8) {
+          float pv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            a[u] = fmaxf(a[u], s[c + u]);
+            pv[u] = fast_exp2(fmaf(s[c + u], scale_log2, nm));
+            rr[u] += pv[u];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])),
+                               fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7]))) * scale_log2;
+        if (__all_sync(0xffffffffu, mt <= m_ref + kRescaleThreshold)) {
+          tmem_st32(tS, p);
+          tmem_st32(tS + 32, p + 32);
+          l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+          done = true;
+        } else {
+          tmem_ld128(tS, s);  // S is still intact in TMEM (P not stored yet)
+        }
       }
-      l += (r0 + r1) + (r2 + r3);
+      if (!done) {
+        float mt;
+        if (full) {
+          // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+          if (scale_log2 >= 0.f) {
+#pragma unroll
+            for (int c = 4; c < kBN; c += 4) {
+              a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
+              a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
+            }
+            mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+          } else {
+#pragma unroll
+            for (int c = 4; c < kBN; c += 4) {
+              a0 = fminf(a0, s[c]); a1 = fminf(a1, s[c + 1]);
+              a2 = fminf(a2, s[c + 2]); a3 = fminf(a3, s[c + 3]);
+            }
+            mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
+          }
+        } else {
+          mt = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            s[c] = (c < nvalid) ? s[c] * scale_log2 : -INFINITY;
+            mt = fmaxf(mt, s[c]);
+          }
+        }
+        const float m_new = fmaxf(m_ref, mt);
+        resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
+        if (resc) {
+          alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // P = 2^(t - m), packed to bf16 pairs and written over the S columns
+        // in two halves of 64 keys (32 TMEM columns each).
+        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t p[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const int k = h * 64 + c;
+            float p0, p1, p2, p3;
+            if (full) {
+              p0 = fast_exp2(fmaf(s[k], scale_log2, -m_use));
+              p1 = fast_exp2(fmaf(s[k + 1], scale_log2, -m_use));
+              p2 = fast_exp2(fmaf(s[k + 2], scale_log2, -m_use));
+              p3 = fast_exp2(fmaf(s[k + 3], scale_log2, -m_use));
+            } else {
+              p0 = fast_exp2(s[k] - m_use);
+              p1 = fast_exp2(s[k + 1] - m_use);
+              p2 = fast_exp2(s[k + 2] - m_use);
+              p3 = fast_exp2(s[k + 3] - m_use);
+            }
+            r0 += p0; r1 += p1; r2 += p2; r3 += p3;
+            p[c / 2] = pack_bf16x2(p0, p1);
+            p[c / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st32(tS + h * 32, p);
+        }
+        l += (r0 + r1) + (r2 + r3);
+      }
 
       // Lazy correction of O: needed only if some row of this warp moved its
       // reference, and only once PV_{j-1} has landed in TMEM.
