@@ -280,8 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
-      float s[kBN];
-      tmem_ld128(tS, s);
+      float s[kBN];  // the S row (slow path only)
 
       const int nvalid = lim - j * kBN;  // keys k < nvalid of this block are visible
       const bool full = nvalid >= kBN;
@@ -297,37 +296,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool done = false;
       if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
         uint32_t p[kBN / 2];
-        float a[8], rr[8];
+        float a[4], rr[8];
         const float nm = -m_ref;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          a[u] = s[u];
-          rr[u] = 0.f;
-        }
+        for (int u = 0; u < 4; ++u) a[u] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 8) {
-          float pv[8];
+        for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+        // two halves of 64 columns keep only half of the row live at a time
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            a[u] = fmaxf(a[u], s[c + u]);
-            pv[u] = fast_exp2(fmaf(s[c + u], scale_log2, nm));
-            rr[u] += pv[u];
+        for (int h = 0; h < 2; ++h) {
+          float sh[64];
+          tmem_ld64(tS + h * 64, sh);
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            // 3-input max folds two new scores per instruction (4 chains)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] = fmax3(a[u], sh[c + u], sh[c + 4 + u]);
+            float tv[8], pv[8];
+#pragma unroll
+            for (int u = 0; u < 8; u += 2)
+              ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) p[(h * 64 + c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
           }
-#pragma unroll
-          for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
         }
-        const float mt = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])),
-                               fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7]))) * scale_log2;
+        const float mt = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) * scale_log2;
         if (__all_sync(0xffffffffu, mt <= m_ref + kRescaleThreshold)) {
           tmem_st32(tS, p);
           tmem_st32(tS + 32, p + 32);
           l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
           done = true;
-        } else {
-          tmem_ld128(tS, s);  // S is still intact in TMEM (P not stored yet)
         }
       }
       if (!done) {
+        tmem_ld128(tS, s);  // S is intact in TMEM (no P stored for this block)
         float mt;
         if (full) {
           // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
