@@ -196,6 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, D, false, true);
+      // Base descriptors are built once; each MMA then adds a compile-time
+      // offset to the 14-bit start-address field (which never carries: every
+      // shared address is below 256 KB), keeping the issue loop short.
+      const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(sRing, 16, 1024);
+      const uint64_t vd0 = sdesc_sw128(sRing, kAtomBytes, 1024);
       bool ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
       tc_fence_after();
 
@@ -207,13 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kSiteKvFull, idx))
           return false;
         tc_fence_after();
-        const uint32_t qb = sQ + t * C::kTileBytes;
-        const uint32_t kb = sRing + slot * C::kTileBytes;
+        const uint64_t qb = qd0 + (uint64_t)(t * (C::kTileBytes >> 4));
+        const uint64_t kb = kd0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const uint32_t dS = tbase + C::kColS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_ss(tbase + C::kColS + t * 128, sdesc_sw128(qb + off, 16, 1024),
-                 sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+          mma_ss(dS, qb + off, kb + off, kIdescS, kk > 0);
         }
         tc_commit(bar_s_full(t));
         const int last_t = (j < Tt[1]) ? 1 : 0;
@@ -230,14 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kSiteKvFull, idx))
           return false;
         tc_fence_after();
-        const uint32_t vb = sRing + slot * C::kTileBytes;
+        const uint64_t vb = vd0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const uint32_t dO = tbase + C::kColO + t * 128;
+        const uint32_t aP = tbase + C::kColS + t * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
           // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
-          mma_ts(tbase + C::kColO + t * 128, tbase + C::kColS + t * 128 + kk * 8,
-                 sdesc_sw128(vb + kk * 16 * 128, kAtomBytes, 1024), kIdescPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                 kk > 0 ? 1u : acc0);
         }
         tc_commit(bar_pv_done(t));
         const int last_t = (j < Tt[1]) ? 1 : 0;
