@@ -18,15 +18,17 @@
 //     columns [0,256) plus the 64 RoPE columns, rank 1 owns [256,512).  Each
 //     CTA TMA-loads only its own columns of every cached row (HBM is read
 //     once) and computes a partial S over them with its share of q held in
-//     TMEM.  The partial S tiles are pushed into the peer's shared memory with
-//     st.async (arrival counted in bytes on the peer's mbarrier, so no thread
-//     issues a cluster-scope fence), both CTAs add them in the same order and
-//     run the identical softmax, and each accumulates its 256 columns of
-//     O = P V in TMEM (V is the same shared-memory bytes as K).
+//     TMEM.  Four exchange warps push each partial S tile into the peer's
+//     shared memory with st.async (arrival counted in bytes on the peer's
+//     mbarrier, so no thread issues a cluster-scope fence); the four softmax
+//     warps add the two partials in the same order on both CTAs and run the
+//     identical softmax; each CTA accumulates its 256 columns of O = P V in
+//     TMEM (V is the same shared-memory bytes as K).
 //   * Pages of 64 tokens are consumed as two 32-token steps through a 7-stage
 //     TMA ring; the block table is read on the device and bounds-checked.
 //     Three S buffers let the tensor core run up to three steps ahead of the
-//     softmax, and the softmax sends step i+1 before finishing step i.
+//     softmax.  Warps: 0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer,
+//     6-9 partial-S exchange.
 //   * Work is a list of page ranges ("chunks") of the flat page order, one
 //     chunk per cluster at a time (persistent).  The device planner either
 //     gives each sequence its own chunk (no partials) or cuts the flat order
@@ -47,31 +49,34 @@ constexpr int kHq = 128;
 constexpr int kDk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
-constexpr int kStep = 32;                 // tokens per pipeline step (half page)
-constexpr int kThreads = 192;             // 4 softmax warps + producer + MMA
+constexpr int kStep = 64;                 // tokens per MMA step (one page)
+constexpr int kHalf = 32;                 // tokens per partial-S exchange
+constexpr int kThreads = 320;             // softmax, producer, MMA, exchange warps
 constexpr int kMaxAtoms = 5;              // 64-column atoms per CTA (rank 0)
-constexpr int kKAtomBytes = kStep * 128;  // 32 tokens x 64 bf16
-constexpr int kStageBytes = kMaxAtoms * kKAtomBytes;  // 20 KB
-constexpr int kStages = 7;
-constexpr int kSBufs = 3;                 // TMEM S buffers
-constexpr int kXBufs = 4;                 // partial-S receive buffers
+constexpr int kQAtomBytes = kHq * 128;    // 128 heads x 64 bf16
+constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
+constexpr int kStageBytes = kMaxAtoms * kKAtomBytes;  // 40 KB
+constexpr int kStages = 3;
+constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
+constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
 constexpr int kXRow = 36;                 // floats per receive row (32 + pad)
 constexpr int kXBufBytes = kHq * kXRow * 4;
-constexpr uint32_t kXBytes = kHq * kStep * 4;  // payload per step
+constexpr uint32_t kXBytes = kHq * kHalf * 4;  // payload per half step
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kStageOff = 0;
+constexpr int kQropeOff = 0;             // rank 0: q's RoPE atom (A of 4 S MMAs)
+constexpr int kStageOff = kQropeOff + kQAtomBytes;
 constexpr int kXOff = kStageOff + kStages * kStageBytes;
 constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
-// barriers: kv_full[S], kv_empty[S], s_full[3], p_full[3], xfull[4], q_full,
-// q_free, pv_done, o_free, mma_drain, o_ready
-constexpr int kNumBars = 2 * kStages + 2 * kSBufs + kXBufs + 6;
+// barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], s_read[2],
+// xfull[4], b_read[2], q_full, q_free, pv_done, o_free, mma_drain, o_ready
+constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
-constexpr uint32_t kColQ = 256;   // up to 160 columns (5 atoms x 32)
-constexpr uint32_t kColS = 416;   // 3 x 32 columns
+constexpr uint32_t kColQ = 256;   // 128 columns: q's four c_kv atoms (bf16 pairs)
+constexpr uint32_t kColS = 384;   // 2 x 64 columns
 
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
@@ -287,6 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return rank == 0 ? (a < 4 ? a * 64 : 512) : (256 + a * 64);
   };
 
+  const uint32_t sQrope = base + kQropeOff;
   const uint32_t sStage = base + kStageOff;
   const uint32_t sX = base + kXOff;
   const uint32_t bar0 = base + kBarOff;
@@ -294,8 +300,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar_kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto bar_s_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
   auto bar_p_full = [&](int b) { return bar0 + 8u * (2 * kStages + kSBufs + b); };
-  auto bar_xfull = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kSBufs + b); };
-  const uint32_t bar_q_full = bar0 + 8u * (2 * kStages + 2 * kSBufs + kXBufs);
+  auto bar_s_read = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kSBufs + b); };
+  auto bar_xfull = [&](int b) { return bar0 + 8u * (2 * kStages + 3 * kSBufs + b); };
+  auto bar_b_read = [&](int b) { return bar0 + 8u * (2 * kStages + 3 * kSBufs + kXBufs + b); };
+  const uint32_t bar_q_full = bar0 + 8u * (2 * kStages + 3 * kSBufs + kXBufs + kSBufs);
   const uint32_t bar_q_free = bar_q_full + 8;
   const uint32_t bar_pv_done = bar_q_full + 16;
   const uint32_t bar_o_free = bar_q_full + 24;
@@ -317,8 +325,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar_s_full(b), 1);
       mbar_init(bar_p_full(b), 128);
+      mbar_init(bar_s_read(b), 128);
     }
     for (int b = 0; b < kXBufs; ++b) mbar_init(bar_xfull(b), 1);
+    for (int b = 0; b < kSBufs; ++b) mbar_init(bar_b_read(b), 128);
     mbar_init(bar_q_full, 128);
     mbar_init(bar_q_free, 1);
     mbar_init(bar_pv_done, 1);
@@ -327,7 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_o_ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // arm the receive barriers for steps 0..3 (re-armed after each use)
+    // arm the receive barriers for half steps 0..3 (re-armed after each use)
     for (int b = 0; b < kXBufs; ++b) mbar_arrive_expect_tx(bar_xfull(b), kXBytes);
     prefetch_tmap(&tmKV);
   }
@@ -387,10 +397,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16(kHq, kStep, false, false);
+      constexpr uint32_t kIdescS = idesc_bf16(kHq, kStep, false, false);  // N = 64 tokens
       constexpr uint32_t kIdescPV = idesc_bf16(kHq, 256, false, true);
       const uint32_t tO = tbase + kColO;
       const uint32_t tQ = tbase + kColQ;
+      // Descriptors are built once; per MMA only the start address moves
+      // (the 14-bit address field never carries into the other fields).
+      const uint64_t kdesc0 = sdesc_sw128(sStage, 16, 1024);
+      const uint64_t qrdesc = sdesc_sw128(sQrope, 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(sStage, kKAtomBytes, 1024);
       int g = 0, seg_i = 0;
       bool ok = true;
       // S partial for global step gg: A = this CTA's q columns (TMEM), B = K atoms.
@@ -399,13 +414,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar_kv_full(slot), (gg / kStages) & 1, abort_flag, err, kSiteKvFull, gg))
           return false;
         tc_fence_after();
-        const uint32_t kb = sStage + slot * kStageBytes;
-        const uint32_t tS = tbase + kColS + (gg % kSBufs) * 32;
-        for (int a = 0; a < natoms; ++a) {
+        const uint64_t kd = kdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
+        const uint32_t tS = tbase + kColS + (gg % kSBufs) * 64;
+        // c_kv atoms: q from TMEM; rank 0's RoPE atom: q from shared memory
+        for (int a = 0; a < 4; ++a) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tS, tQ + a * 32 + kk * 8, sdesc_sw128(kb + a * kKAtomBytes + kk * 32, 16, 1024),
+            mma_ts(tS, tQ + a * 32 + kk * 8, kd + (uint64_t)((a * kKAtomBytes + kk * 32) >> 4),
                    kIdescS, (a | kk) != 0);
+        }
+        if (natoms == 5) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4),
+                   kd + (uint64_t)((4 * kKAtomBytes + kk * 32) >> 4), kIdescS, 1u);
         }
         tc_commit(bar_s_full(gg % kSBufs));
         return true;
@@ -431,12 +453,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int slot = gi % kStages;
-            const uint32_t vb = sStage + slot * kStageBytes;
+            const uint64_t vd = vdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kStep / 16; ++kk)
-              mma_ts(tO, tbase + kColS + (gi % kSBufs) * 32 + kk * 8,
-                     sdesc_sw128(vb + kk * 16 * 128, kKAtomBytes, 1024), kIdescPV,
-                     (i > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tO, tbase + kColS + (gi % kSBufs) * 64 + kk * 8,
+                     vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar_kv_empty(slot));
             tc_commit(bar_pv_done);
             if (i == n - 1) tc_commit(bar_o_ready);
@@ -454,15 +475,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait(bar_mma_drain, 0, &never, nullptr, kSiteDrain, -2);
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ================= exchange warps (6-9): own partial S -> peer ===========
+    // Step k is sent (as two 32-token halves) once S(k) is in TMEM and this
+    // CTA's softmax warps have read the peer's step k-1: the peer cannot then
+    // reach a receive buffer that is still being read here.
+    const int r = (warp & 3) * 32 + lane;  // head == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS0 = tbase + lane_off + kColS;
+    const uint32_t peer_row = mapa_shared(sX + r * kXRow * 4, peer);
+    const uint32_t peer_xfull0 = mapa_shared(bar_xfull(0), peer);
+    int total = 0;
+    for (int k = cluster; k < nchunks; k += nclusters) {
+      ChunkIter it;
+      it.init(prefix, bounds, B, k);
+      Seg s;
+      while (it.next(s)) total += seg_steps(s.p0, s.p1, seqlens[s.b]);
+    }
+    for (int gg = 0; gg < total; ++gg) {
+      const int sb = gg % kSBufs;
+      bool w = mbar_wait(bar_s_full(sb), (gg / kSBufs) & 1, abort_flag, err, kSiteSFull, gg);
+      if (w && gg > 0) {
+        const int pb = (gg - 1) % kSBufs;
+        w = mbar_wait(bar_b_read(pb), ((gg - 1) / kSBufs) & 1, abort_flag, err, kSiteXfree, gg);
+      }
+      w = __all_sync(0xffffffffu, w);
+      if (!w) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float sv[kHalf];
+        tmem_ld32(tS0 + sb * 64 + h * 32, sv);
+        const int xb = (2 * gg + h) % kXBufs;
+        const uint32_t dst = peer_row + xb * kXBufBytes;
+        const uint32_t rbar = peer_xfull0 + 8u * xb;
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 4)
+          st_async_v4(dst + c * 4, __float_as_uint(sv[c]), __float_as_uint(sv[c + 1]),
+                      __float_as_uint(sv[c + 2]), __float_as_uint(sv[c + 3]), rbar);
+      }
+      tc_fence_before();
+      mbar_arrive(bar_s_read(sb));
+    }
   } else {
-    // ================= softmax, exchange, epilogue (warps 0-3) ============
+    // ================= softmax and epilogue (warps 0-3) ============
     const int r = threadIdx.x;  // head == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tbase + lane_off + kColO;
     const uint32_t tQ = tbase + lane_off + kColQ;
     const uint32_t tS0 = tbase + lane_off + kColS;
-    const uint32_t peer_row = mapa_shared(sX + r * kXRow * 4, peer);
-    const uint32_t peer_xfull0 = mapa_shared(bar_xfull(0), peer);
     const float* my_row = reinterpret_cast<const float*>(smem + kXOff + r * kXRow * 4);
     constexpr float kLn2 = 0.69314718055994530942f;
     int g = 0, seg_i = 0;
@@ -470,24 +531,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the previous segment, whose epilogue runs once the next q is in place
     int prev_b = -1, prev_slot = -1, prev_seg = 0;
     float prev_m = 0.f, prev_l = 0.f;
-
-    // A(gg): own partial S of step gg -> registers, and pushed to the peer.
-    auto stepA = [&](int gg, float* sv) -> bool {
-      const int sb = gg % kSBufs;
-      bool w = mbar_wait(bar_s_full(sb), (gg / kSBufs) & 1, abort_flag, err, kSiteSFull, gg);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) return false;
-      tc_fence_after();
-      tmem_ld32(tS0 + sb * 32, sv);
-      const int xb = gg % kXBufs;
-      const uint32_t dst = peer_row + xb * kXBufBytes;
-      const uint32_t rbar = peer_xfull0 + 8u * xb;
-#pragma unroll
-      for (int c = 0; c < kStep; c += 4)
-        st_async_v4(dst + c * 4, __float_as_uint(sv[c]), __float_as_uint(sv[c + 1]),
-                    __float_as_uint(sv[c + 2]), __float_as_uint(sv[c + 3]), rbar);
-      return true;
-    };
 
     auto epilogue = [&]() {
       // O / l -> bf16 (whole sequence) or fp32 partial; LSE from rank 0
@@ -542,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         {
           const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + r) * kDk);
-          for (int a = 0; a < natoms; ++a) {
+          for (int a = 0; a < 4; ++a) {
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -550,6 +593,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
             }
             tmem_st32(tQ + a * 32, w);
+          }
+          if (natoms == 5) {
+            // RoPE atom -> shared memory, 128-byte swizzled rows (K-major A)
+            uint8_t* qr = smem + kQropeOff + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(qr + ((c ^ (r & 7)) * 16)) = __ldg(qrow + 512 / 8 + c);
+            fence_proxy_async_smem();
           }
           tmem_st_wait();
           tc_fence_before();
@@ -564,46 +615,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           epilogue();
           prev_b = -1;
         }
-        // ---- steps: send step i+1 before finishing step i
         float m_ref = -INFINITY, l = 0.f;
-        float scur[kStep];
-        ok = stepA(g, scur);
         for (int i = 0; i < n && ok; ++i) {
           const int gi = g + i;
-          float snext[kStep];
-          if (i + 1 < n) {
-            ok = stepA(gi + 1, snext);
-            if (!ok) break;
-          }
-          // peer's partial of step gi -> full S (same sum order on both CTAs)
-          const int xb = gi % kXBufs;
-          ok = mbar_wait<true>(bar_xfull(xb), (gi / kXBufs) & 1, abort_flag, err, kSiteXchg, gi);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          const float* xin = my_row + xb * (kXBufBytes / 4);
+          const int sb = gi % kSBufs;
+          // peer's partial of step gi, two 32-token halves (pushed by its
+          // exchange warps)
+          float px[kStep];
 #pragma unroll
-          for (int c = 0; c < kStep; c += 4) {
-            const float4 pv = *reinterpret_cast<const float4*>(xin + c);
-            if (rank == 0) {
-              scur[c] += pv.x; scur[c + 1] += pv.y; scur[c + 2] += pv.z; scur[c + 3] += pv.w;
-            } else {
-              scur[c] = pv.x + scur[c]; scur[c + 1] = pv.y + scur[c + 1];
-              scur[c + 2] = pv.z + scur[c + 2]; scur[c + 3] = pv.w + scur[c + 3];
+          for (int h = 0; h < 2; ++h) {
+            const int xb = (2 * gi + h) % kXBufs;
+            ok = mbar_wait<true>(bar_xfull(xb), ((2 * gi + h) / kXBufs) & 1, abort_flag, err,
+                                 kSiteXchg, gi);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const float* xin = my_row + xb * (kXBufBytes / 4);
+#pragma unroll
+            for (int c = 0; c < kHalf; c += 4) {
+              const float4 pv = *reinterpret_cast<const float4*>(xin + c);
+              px[h * 32 + c] = pv.x; px[h * 32 + c + 1] = pv.y;
+              px[h * 32 + c + 2] = pv.z; px[h * 32 + c + 3] = pv.w;
             }
           }
-          // Re-arm this receive buffer for step gi + 4.  The peer can only
-          // send that step after this CTA has sent step gi + 2, which every
-          // thread does after this read.
-          if (r == 0) mbar_arrive_expect_tx(bar_xfull(xb), kXBytes);
-
-          // ---- mask tokens at or past the sequence end, online softmax
-          const int nvalid = L - (t0 + i * kStep);
-          float mt = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kStep; ++c) {
-            scur[c] = (c < nvalid) ? scur[c] * scale_log2 : -INFINITY;
-            mt = fmaxf(mt, scur[c]);
+          if (!ok) break;
+          mbar_arrive(bar_b_read(sb));  // the loads above have returned their values
+          // Re-arm both half-buffers for step gi + 2.  The peer can only send
+          // that step after this CTA has sent step gi + 1, which waits for
+          // every thread's b_read of this step.
+          if (r == 0) {
+            mbar_arrive_expect_tx(bar_xfull((2 * gi) % kXBufs), kXBytes);
+            mbar_arrive_expect_tx(bar_xfull((2 * gi + 1) % kXBufs), kXBytes);
           }
+          // own partial of step gi
+          ok = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull, gi);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          float sv[kStep];
+          tmem_ld64(tS0 + sb * 64, sv);
+          // full S in the same summation order on both CTAs (rank 0 + rank 1)
+          const int nvalid = L - (t0 + i * kStep);
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kStep; c += 4) {
+            float t4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float full = (rank == 0) ? (sv[c + u] + px[c + u]) : (px[c + u] + sv[c + u]);
+              t4[u] = (c + u < nvalid) ? full * scale_log2 : -INFINITY;
+              sv[c + u] = t4[u];
+            }
+            mx0 = fmaxf(mx0, t4[0]); mx1 = fmaxf(mx1, t4[1]);
+            mx2 = fmaxf(mx2, t4[2]); mx3 = fmaxf(mx3, t4[3]);
+          }
+          const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
           const float m_new = fmaxf(m_ref, mt);
           const bool resc = m_new > m_ref + kRescaleThreshold;
           float alpha = 1.f;
@@ -614,24 +679,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           uint32_t p[kStep / 2];
-          float rs0 = 0.f, rs1 = 0.f;
+          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-          for (int c = 0; c < kStep; c += 2) {
-            const float p0 = fast_exp2(scur[c] - m_use);
-            const float p1 = fast_exp2(scur[c + 1] - m_use);
-            rs0 += p0;
-            rs1 += p1;
+          for (int c = 0; c < kStep; c += 4) {
+            const float p0 = fast_exp2(sv[c] - m_use);
+            const float p1 = fast_exp2(sv[c + 1] - m_use);
+            const float p2 = fast_exp2(sv[c + 2] - m_use);
+            const float p3 = fast_exp2(sv[c + 3] - m_use);
+            rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
             p[c / 2] = pack_bf16x2(p0, p1);
+            p[c / 2 + 1] = pack_bf16x2(p2, p3);
           }
-          l += rs0 + rs1;
-          tmem_st16(tS0 + (gi % kSBufs) * 32, p);
+          l += (rs0 + rs1) + (rs2 + rs3);
           // Tokens past the end contribute exactly zero even if the cache
           // tail holds non-finite bytes: clear those V rows before PV reads.
           // Each thread fences its own writes; the PV MMA is issued only after
           // all 128 threads have arrived on p_full below.
           if (nvalid < kStep) {
             uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
-            const int zrows = kStep - nvalid;  // rows [nvalid, 32) of atoms 0..3
+            const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
             for (int e = threadIdx.x; e < zrows * 4 * 8; e += 128) {
               const int a = e / (zrows * 8), rem = e % (zrows * 8);
               const int rr = nvalid + rem / 8, ch = rem % 8;
@@ -655,11 +721,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tmem_st32(tO + c, ou);
             }
           }
+          // P overwrites the S buffer: the exchange warps must have read it
+          ok = mbar_wait(bar_s_read(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull, gi);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          tmem_st32(tS0 + sb * 64, p);
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(bar_p_full(gi % kSBufs));
-#pragma unroll
-          for (int c = 0; c < kStep; ++c) scur[c] = snext[c];
+          mbar_arrive(bar_p_full(sb));
         }
         if (!ok) break;
         prev_b = s.b;
