@@ -24,11 +24,12 @@
 //     warps add the two partials in the same order on both CTAs and run the
 //     identical softmax; each CTA accumulates its 256 columns of O = P V in
 //     TMEM (V is the same shared-memory bytes as K).
-//   * Pages of 64 tokens are consumed as two 32-token steps through a 7-stage
-//     TMA ring; the block table is read on the device and bounds-checked.
-//     Three S buffers let the tensor core run up to three steps ahead of the
-//     softmax.  Warps: 0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer,
-//     6-9 partial-S exchange.
+//   * Each 64-token page is one step (S MMAs with N=64) through a 3-stage TMA
+//     ring; the block table is read on the device and bounds-checked.  Two S
+//     buffers in TMEM let the tensor core compute step g+1 while the softmax
+//     of step g runs; the partial S travels in two 32-token halves.  Warps:
+//     0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer, 6-9 partial-S
+//     exchange.
 //   * Work is a list of page ranges ("chunks") of the flat page order, one
 //     chunk per cluster at a time (persistent).  The device planner either
 //     gives each sequence its own chunk (no partials) or cuts the flat order
