@@ -17,16 +17,22 @@
 //               32 KB slots (128-byte swizzle), full/empty mbarriers per slot.
 //   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
 //               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
-//               O_t += P_t V_j with P read straight from TMEM as the A operand.
-//               The issue order S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, ... lets
-//               the tensor core work on one tile while the other tile's
-//               softmax runs (ping-pong).
+//               O_t += P_t V_j with P read straight from TMEM as the A operand,
+//               in two halves of 64 keys.  The issue order S0_0, S1_0, PV0_0,
+//               S0_1, PV1_0, S1_1, ... lets the tensor core work on one tile
+//               while the other tile's softmax runs (ping-pong).
 //   * warps 0-3 / 4-7 : softmax warpgroup of tile 0 / tile 1, one thread per
-//               query row (TMEM lane = row): load the S row, mask, running max,
-//               exp2, row sum, write P (bf16) over the S columns, rescale O in
-//               TMEM only when the max grew by more than 2^8 (lazy rescale;
-//               exact because O and l share the stale reference), and finally
-//               O/l -> bf16 -> smem -> TMA store, plus LSE.
+//               query row (TMEM lane = row).  Each block's 128 keys are taken
+//               as two online-softmax steps of 64 keys: load the S half, mask,
+//               exp2, row sum, write P (bf16) over already-read S columns and
+//               hand that half to the MMA thread at once, so the PV of the
+//               first half runs while the second half is computed.  The fast
+//               path computes P with the current reference and no row max; it
+//               is kept while every half-row sum is at most 2^16 (so every P
+//               is), otherwise the half is redone with its exact max.  O in
+//               TMEM is rescaled only when the max grew by more than 2^8 (lazy
+//               rescale; exact because O and l share the stale reference), and
+//               finally O/l -> bf16 -> smem -> TMA store, plus LSE.
 //   TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 //   Work order: heads in groups of 16 (the CTAs running together share those
 //   heads' K/V in L2), heaviest causal Q pairs first within a group.
@@ -46,6 +52,7 @@ constexpr int kTilesPerCta = 2;
 constexpr int kThreads = 320;         // 2 softmax warpgroups + producer + MMA
 constexpr int kAtomBytes = 128 * 128; // one 128-row x 64-col bf16 swizzle column
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kFastSumLimit = 65536.0f;   // fast path kept while every half-row sum <= 2^16
 constexpr int kHeadGroup = 16;             // heads scheduled together
 
 template <int D>
@@ -56,9 +63,10 @@ struct Cfg {
   static constexpr int kQOff = 0;                          // Q0, Q1
   static constexpr int kRingOff = kTilesPerCta * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2],
-  // pv_done[2], mma_drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[tile], p_full[tile][half],
+  // pv_done[tile][half], mma_drain.  The per-half barriers each complete once
+  // per KV block, so no waiter is ever two phases behind or ahead of one.
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 4 + 4 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
@@ -87,9 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_kv_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
   auto bar_s_full = [&](int t) { return bar0 + 8u * (1 + 2 * C::kStages + t); };
-  auto bar_p_full = [&](int t) { return bar0 + 8u * (3 + 2 * C::kStages + t); };
-  auto bar_pv_done = [&](int t) { return bar0 + 8u * (5 + 2 * C::kStages + t); };
-  const uint32_t bar_mma_drain = bar0 + 8u * (7 + 2 * C::kStages);
+  auto bar_p_full = [&](int t, int h) { return bar0 + 8u * (3 + 2 * C::kStages + 2 * t + h); };
+  auto bar_pv_done = [&](int t, int h) { return bar0 + 8u * (7 + 2 * C::kStages + 2 * t + h); };
+  const uint32_t bar_mma_drain = bar0 + 8u * (11 + 2 * C::kStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -128,8 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s_full(t), 1);
-      mbar_init(bar_p_full(t), 128);
-      mbar_init(bar_pv_done(t), 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(bar_p_full(t, h), 128);
+        mbar_init(bar_pv_done(t, h), 1);
+      }
     }
     mbar_init(bar_mma_drain, 1);
     *abort_flag = 0;
@@ -226,28 +236,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == last_t) tc_commit(bar_kv_empty(slot));
         return true;
       };
-      // O_t += P_t V_j once the softmax of tile t has written P_t.
+      // O_t += P_t V_j in two halves of 64 keys: the softmax of tile t hands
+      // each half h of P_t over on p_full[t][h], and that half's MMAs are
+      // committed to pv_done[t][h] (each completes once per block).
       auto issue_pv = [&](int t, int j) -> bool {
-        if (!mbar_wait(bar_p_full(t), j & 1, abort_flag, err, kSitePFull, j)) return false;
-        tc_fence_after();
         const int idx = 2 * j + 1;
         const int slot = idx % C::kStages;
-        if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
-                       kSiteKvFull, idx))
-          return false;
-        tc_fence_after();
         const uint64_t vb = vd0 + (uint64_t)(slot * (C::kTileBytes >> 4));
         const uint32_t dO = tbase + C::kColO + t * 128;
         const uint32_t aP = tbase + C::kColS + t * 128;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
-          // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
-          mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                 kk > 0 ? 1u : acc0);
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(bar_p_full(t, h), j & 1, abort_flag, err, kSitePFull, 2 * j + h))
+            return false;
+          tc_fence_after();
+          if (h == 0) {
+            if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
+                           kSiteKvFull, idx))
+              return false;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
+            // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
+            // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
+            mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                   kk > 0 ? 1u : acc0);
+          }
+          tc_commit(bar_pv_done(t, h));
         }
-        tc_commit(bar_pv_done(t));
         const int last_t = (j < Tt[1]) ? 1 : 0;
         if (t == last_t) tc_commit(bar_kv_empty(slot));
         return true;
@@ -288,38 +306,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
-      float s[kBN];  // the S row (slow path only)
-
-      const int nvalid = lim - j * kBN;  // keys k < nvalid of this block are visible
-      const bool full = nvalid >= kBN;
-      float alpha = 1.f;
-      bool resc = false;
-      // Fast path (block fully visible, reference already set, scale >= 0):
-      // P = 2^(scale*s - m_ref) is computed with the CURRENT reference while
-      // the row max is reduced alongside, so the max is off the critical
-      // path.  The result is kept unless the max grew by more than 2^8 (rare
-      // after the first block); then S is reloaded from TMEM and the block is
-      // redone on the slow path below.  Both give the same P (the row sum
-      // differs only in its rounding order).
-      bool done = false;
-      if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
-        uint32_t p[kBN / 2];
-        float a[4], rr[8];
-        const float nm = -m_ref;
+      // Each 64-key half of the block is an online-softmax step of its own:
+      // its P is handed to the MMA thread as soon as it is written, so the PV
+      // MMAs of the first half run while the second half is computed.
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int nvalid = lim - j * kBN - h * 64;  // keys c < nvalid of this half are visible
+        const bool full = nvalid >= 64;
+        const uint32_t tSh = tS + h * 64;  // this half's 64 S columns
+        const uint32_t tPh = tS + h * 32;  // its P (bf16 pairs, over already-read S columns)
+        float alpha = 1.f;
+        bool resc = false;
+        uint32_t p[32];
+        // Fast path (half fully visible, reference set, scale >= 0): P =
+        // 2^(scale*s - m_ref) with the CURRENT reference and no row max.  It
+        // is kept when every row sum of the half is at most kFastSumLimit,
+        // which bounds every P by that limit; otherwise S, still intact in
+        // TMEM, is reloaded and the half takes the slow path with its max.
+        bool done = false;
+        if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
+          float sh[64], rr[8];
+          const float nm = -m_ref;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) rr[u] = 0.f;
-        // two halves of 64 columns keep only half of the row live at a time
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float sh[64];
-          tmem_ld64(tS + h * 64, sh);
+          for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+          tmem_ld64(tSh, sh);
 #pragma unroll
           for (int c = 0; c < 64; c += 8) {
-            // 3-input max folds two new scores per instruction (4 chains)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) a[u] = fmax3(a[u], sh[c + u], sh[c + 4 + u]);
             float tv[8], pv[8];
 #pragma unroll
             for (int u = 0; u < 8; u += 2)
@@ -329,108 +341,107 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
 #pragma unroll
-            for (int u = 0; u < 8; u += 2) p[(h * 64 + c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+            for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+          }
+          const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+          if (__all_sync(0xffffffffu, rs <= kFastSumLimit)) {
+            tmem_st32(tPh, p);
+            l += rs;
+            done = true;
           }
         }
-        const float mt = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) * scale_log2;
-        if (__all_sync(0xffffffffu, mt <= m_ref + kRescaleThreshold)) {
-          tmem_st32(tS, p);
-          tmem_st32(tS + 32, p + 32);
-          l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
-          done = true;
-        }
-      }
-      if (!done) {
-        tmem_ld128(tS, s);  // S is intact in TMEM (no P stored for this block)
-        float mt;
-        if (full) {
-          // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-          if (scale_log2 >= 0.f) {
+        if (!done) {
+          float sv[64];
+          tmem_ld64(tSh, sv);  // S of this half is intact (no P stored over it yet)
+          float mt;
+          if (full) {
+            // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
+            float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
+            if (scale_log2 >= 0.f) {
 #pragma unroll
-            for (int c = 4; c < kBN; c += 4) {
-              a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
-              a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
+              for (int c = 4; c < 64; c += 4) {
+                a0 = fmaxf(a0, sv[c]); a1 = fmaxf(a1, sv[c + 1]);
+                a2 = fmaxf(a2, sv[c + 2]); a3 = fmaxf(a3, sv[c + 3]);
+              }
+              mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+            } else {
+#pragma unroll
+              for (int c = 4; c < 64; c += 4) {
+                a0 = fminf(a0, sv[c]); a1 = fminf(a1, sv[c + 1]);
+                a2 = fminf(a2, sv[c + 2]); a3 = fminf(a3, sv[c + 3]);
+              }
+              mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
             }
-            mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
           } else {
+            mt = -INFINITY;
 #pragma unroll
-            for (int c = 4; c < kBN; c += 4) {
-              a0 = fminf(a0, s[c]); a1 = fminf(a1, s[c + 1]);
-              a2 = fminf(a2, s[c + 2]); a3 = fminf(a3, s[c + 3]);
+            for (int c = 0; c < 64; ++c) {
+              sv[c] = (c < nvalid) ? sv[c] * scale_log2 : -INFINITY;
+              mt = fmaxf(mt, sv[c]);
             }
-            mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
           }
-        } else {
-          mt = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            s[c] = (c < nvalid) ? s[c] * scale_log2 : -INFINITY;
-            mt = fmaxf(mt, s[c]);
+          const float m_new = fmaxf(m_ref, mt);
+          resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
+          if (resc) {
+            alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
+            m_ref = m_new;
+            l *= alpha;
           }
-        }
-        const float m_new = fmaxf(m_ref, mt);
-        resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
-        if (resc) {
-          alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
-          m_ref = m_new;
-          l *= alpha;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // P = 2^(t - m), packed to bf16 pairs and written over the S columns
-        // in two halves of 64 keys (32 TMEM columns each).
-        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t p[32];
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
-            const int k = h * 64 + c;
             float p0, p1, p2, p3;
             if (full) {
-              p0 = fast_exp2(fmaf(s[k], scale_log2, -m_use));
-              p1 = fast_exp2(fmaf(s[k + 1], scale_log2, -m_use));
-              p2 = fast_exp2(fmaf(s[k + 2], scale_log2, -m_use));
-              p3 = fast_exp2(fmaf(s[k + 3], scale_log2, -m_use));
+              p0 = fast_exp2(fmaf(sv[c], scale_log2, -m_use));
+              p1 = fast_exp2(fmaf(sv[c + 1], scale_log2, -m_use));
+              p2 = fast_exp2(fmaf(sv[c + 2], scale_log2, -m_use));
+              p3 = fast_exp2(fmaf(sv[c + 3], scale_log2, -m_use));
             } else {
-              p0 = fast_exp2(s[k] - m_use);
-              p1 = fast_exp2(s[k + 1] - m_use);
-              p2 = fast_exp2(s[k + 2] - m_use);
-              p3 = fast_exp2(s[k + 3] - m_use);
+              p0 = fast_exp2(sv[c] - m_use);
+              p1 = fast_exp2(sv[c + 1] - m_use);
+              p2 = fast_exp2(sv[c + 2] - m_use);
+              p3 = fast_exp2(sv[c + 3] - m_use);
             }
             r0 += p0; r1 += p1; r2 += p2; r3 += p3;
             p[c / 2] = pack_bf16x2(p0, p1);
             p[c / 2 + 1] = pack_bf16x2(p2, p3);
           }
-          tmem_st32(tS + h * 32, p);
+          tmem_st32(tPh, p);
+          l += (r0 + r1) + (r2 + r3);
         }
-        l += (r0 + r1) + (r2 + r3);
-      }
 
-      // Lazy correction of O: needed only if some row of this warp moved its
-      // reference, and only once PV_{j-1} has landed in TMEM.
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        ok = mbar_wait(bar_pv_done(t), (j - 1) & 1, abort_flag, err, kSitePvDone, j);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
+        // Lazy correction of O before this half's PV: needed only if some row
+        // of this warp moved its reference, and only once every earlier PV of
+        // the tile has landed: the second half of block j-1 (h = 0) or the
+        // first half of block j (h = 1).
+        if ((j > 0 || h > 0) && __any_sync(0xffffffffu, resc)) {
+          ok = h == 0 ? mbar_wait(bar_pv_done(t, 1), (j - 1) & 1, abort_flag, err, kSitePvDone,
+                                  2 * j)
+                      : mbar_wait(bar_pv_done(t, 0), j & 1, abort_flag, err, kSitePvDone,
+                                  2 * j + 1);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          uint32_t ou[32];
+          for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            uint32_t ou[32];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
-          tmem_st32(tO + c * 32, ou);
+            for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
+            tmem_st32(tO + c * 32, ou);
+          }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_p_full(t, h));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_p_full(t));
+      if (!ok) break;
     }
 
     if (T > 0) {
-      if (ok) ok = mbar_wait(bar_pv_done(t), (T - 1) & 1, abort_flag, err, kSitePvDone, T);
+      if (ok) ok = mbar_wait(bar_pv_done(t, 1), (T - 1) & 1, abort_flag, err, kSitePvDone, 2 * T);
       ok = __all_sync(0xffffffffu, ok);
       const uint32_t stage_addr = sQ + t * C::kTileBytes;  // Q_t is no longer read
       if (ok) {
