@@ -193,7 +193,8 @@ ATTN_API const char* attn_last_error(void);
  *
  * Same as attn_fwd with dtype = ATTN_DTYPE_BF16, except that the producer
  * warp of every CTA deliberately never issues K/V load number
- * `skip_load_index` (>= 1, counting K0, V0, K1, V1, ...).  The consumers'
+ * `skip_load_index` (>= 1, counting K0, V0, K1, V1, ...); K_j and V_j share
+ * one pipeline stage, so both loads of that block are skipped.  The consumers'
  * bounded waits then run out (about 2 s), the kernel records
  * ATTN_ERR_DEVICE_TIMEOUT, every CTA unwinds and frees its tensor memory, and
  * attn_device_status() returns the code.  Nothing hangs, faults or traps.

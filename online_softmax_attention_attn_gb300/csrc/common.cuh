@@ -51,6 +51,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   auto probe = [&]() {
     return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
+  // A non-blocking test first: most waits find the phase complete already.
+  if (!kClusterScope && mbar_test_wait(bar, parity)) return true;
   if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {

@@ -13,8 +13,9 @@
 // How it maps onto GB300 (nothing here is taken from the pages' Ampere,
 // Hopper or RTX kernels).  One CTA owns TWO consecutive 128-row Q tiles of
 // one head and streams that head's K/V blocks once for both:
-//   * warp 8  : TMA producer.  Both Q tiles once, then K_j, V_j into a ring of
-//               32 KB slots (128-byte swizzle), full/empty mbarriers per slot.
+//   * warp 8  : TMA producer.  Both Q tiles once, then K_j and V_j together
+//               into a ring of stages (128-byte swizzle), one full and one
+//               empty mbarrier per stage.
 //   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
 //               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
 //               O_t += P_t V_j with P read straight from TMEM as the A operand,
@@ -59,10 +60,11 @@ template <int D>
 struct Cfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kTileBytes = kAtoms * kAtomBytes;  // Q, K or V block
-  static constexpr int kStages = (D == 128) ? 5 : 10;     // ring slots
+  static constexpr int kStageBytes = 2 * kTileBytes;      // K_j then V_j
+  static constexpr int kStages = (D == 128) ? 2 : 5;      // ring slots (one KV block each)
   static constexpr int kQOff = 0;                          // Q0, Q1
   static constexpr int kRingOff = kTilesPerCta * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[tile], p_full[tile][half],
   // pv_done[tile][half], mma_drain.  The per-half barriers each complete once
   // per KV block, so no waiter is ever two phases behind or ahead of one.
@@ -167,34 +169,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full, a * 64,
                       (2 * pr + t) * kBM, bh);
-      int issued_until = 0;  // loads [0, issued_until) were issued
+      int issued_until = 0;  // blocks [0, issued_until) were issued
+      const int skip_block = debug_skip_load > 0 ? debug_skip_load / 2 : -1;  // test hook
       bool ok = true;
-      for (int idx = 0; idx < 2 * Tmax && ok; ++idx) {
-        const int slot = idx % C::kStages;
-        const int use = idx / C::kStages;
+      for (int j = 0; j < Tmax && ok; ++j) {
+        const int slot = j % C::kStages;
+        const int use = j / C::kStages;
         if (use > 0) {
-          ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty,
-                         idx);
+          ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, j);
           if (!ok) break;
         }
-        if (debug_skip_load > 0 && idx == debug_skip_load) continue;  // test hook
-        const int j = idx >> 1;
-        const CUtensorMap* m = (idx & 1) ? &tmV : &tmK;
-        const uint32_t dst = sRing + slot * C::kTileBytes;
-        mbar_arrive_expect_tx(bar_kv_full(slot), C::kTileBytes);
+        if (j == skip_block) continue;
+        // K_j and V_j land on one barrier
+        const uint32_t dst = sRing + slot * C::kStageBytes;
+        mbar_arrive_expect_tx(bar_kv_full(slot), C::kStageBytes);
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d_hint(dst + a * kAtomBytes, m, bar_kv_full(slot), a * 64, j * kBN, bh,
+          tma_load_3d_hint(dst + a * kAtomBytes, &tmK, bar_kv_full(slot), a * 64, j * kBN, bh,
                            pol_kv);
-        issued_until = idx + 1;
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(slot), a * 64,
+                           j * kBN, bh, pol_kv);
+        issued_until = j + 1;
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA unwinds.
         const int first = issued_until > C::kStages ? issued_until - C::kStages : 0;
-        for (int idx = first; idx < issued_until; ++idx) {
-          if (debug_skip_load > 0 && idx == debug_skip_load) continue;
+        for (int j = first; j < issued_until; ++j) {
+          if (j == skip_block) continue;
           volatile int never = 0;
-          mbar_wait(bar_kv_full(idx % C::kStages), (idx / C::kStages) & 1, &never, nullptr,
-                    kSiteDrain, idx);
+          mbar_wait(bar_kv_full(j % C::kStages), (j / C::kStages) & 1, &never, nullptr,
+                    kSiteDrain, j);
         }
         volatile int never = 0;
         mbar_wait(bar_q_full, 0, &never, nullptr, kSiteDrain, -1);
@@ -215,16 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
       tc_fence_after();
 
-      // S_t = Q_t K_j^T; the slot of K_j is released by the last tile using it.
+      // S_t = Q_t K_j^T (its wait also covers V_j, which shares the stage)
       auto issue_s = [&](int t, int j) -> bool {
-        const int idx = 2 * j;
-        const int slot = idx % C::kStages;
-        if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
-                       kSiteKvFull, idx))
+        const int slot = j % C::kStages;
+        if (!mbar_wait(bar_kv_full(slot), (j / C::kStages) & 1, abort_flag, err, kSiteKvFull,
+                       j))
           return false;
         tc_fence_after();
         const uint64_t qb = qd0 + (uint64_t)(t * (C::kTileBytes >> 4));
-        const uint64_t kb = kd0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const uint64_t kb = kd0 + (uint64_t)(slot * (C::kStageBytes >> 4));
         const uint32_t dS = tbase + C::kColS + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -232,17 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(dS, qb + off, kb + off, kIdescS, kk > 0);
         }
         tc_commit(bar_s_full(t));
-        const int last_t = (j < Tt[1]) ? 1 : 0;
-        if (t == last_t) tc_commit(bar_kv_empty(slot));
         return true;
       };
       // O_t += P_t V_j in two halves of 64 keys: the softmax of tile t hands
       // each half h of P_t over on p_full[t][h], and that half's MMAs are
       // committed to pv_done[t][h] (each completes once per block).
       auto issue_pv = [&](int t, int j) -> bool {
-        const int idx = 2 * j + 1;
-        const int slot = idx % C::kStages;
-        const uint64_t vb = vd0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const int slot = j % C::kStages;
+        const uint64_t vb = vd0 + (uint64_t)((slot * C::kStageBytes + C::kTileBytes) >> 4);
         const uint32_t dO = tbase + C::kColO + t * 128;
         const uint32_t aP = tbase + C::kColS + t * 128;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
@@ -251,12 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_p_full(t, h), j & 1, abort_flag, err, kSitePFull, 2 * j + h))
             return false;
           tc_fence_after();
-          if (h == 0) {
-            if (!mbar_wait(bar_kv_full(slot), (idx / C::kStages) & 1, abort_flag, err,
-                           kSiteKvFull, idx))
-              return false;
-            tc_fence_after();
-          }
 #pragma unroll
           for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
             // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
@@ -266,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar_pv_done(t, h));
         }
+        // the stage of block j is free once the last tile reading it is done
         const int last_t = (j < Tt[1]) ? 1 : 0;
         if (t == last_t) tc_commit(bar_kv_empty(slot));
         return true;
