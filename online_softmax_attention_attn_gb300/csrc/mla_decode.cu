@@ -60,9 +60,13 @@ constexpr int kStageBytes = kMaxAtoms * kKAtomBytes;  // 40 KB
 constexpr int kStages = 3;
 constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
-constexpr int kXRow = 36;                 // floats per receive row (32 + pad)
-constexpr int kXBufBytes = kHq * kXRow * 4;
-constexpr uint32_t kXBytes = kHq * kHalf * 4;  // payload per half step
+// A received half is [token quad q][head][4 tokens] fp32: 16 B per head and
+// quad, so one exchange-warp store covers 512 contiguous bytes (32 heads) --
+// contiguous remote stores move about twice the bytes per clock of
+// row-scattered ones -- and each head's reads are conflict-free.
+constexpr int kXQuadBytes = kHq * 16;          // one token quad, all heads
+constexpr int kXBufBytes = (kHalf / 4) * kXQuadBytes;
+constexpr uint32_t kXBytes = kXBufBytes;       // payload per half step
 constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kQropeOff = 0;             // rank 0: q's RoPE atom (A of 4 S MMAs)
@@ -484,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // head == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS0 = tbase + lane_off + kColS;
-    const uint32_t peer_row = mapa_shared(sX + r * kXRow * 4, peer);
+    const uint32_t peer_row = mapa_shared(sX + r * 16, peer);  // this head's 16 B of each quad
     const uint32_t peer_xfull0 = mapa_shared(bar_xfull(0), peer);
     int total = 0;
     for (int k = cluster; k < nchunks; k += nclusters) {
@@ -512,8 +516,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t rbar = peer_xfull0 + 8u * xb;
 #pragma unroll
         for (int c = 0; c < kHalf; c += 4)
-          st_async_v4(dst + c * 4, __float_as_uint(sv[c]), __float_as_uint(sv[c + 1]),
-                      __float_as_uint(sv[c + 2]), __float_as_uint(sv[c + 3]), rbar);
+          st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
+                      __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
+                      __float_as_uint(sv[c + 3]), rbar);
       }
       tc_fence_before();
       mbar_arrive(bar_s_read(sb));
@@ -525,7 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tO = tbase + lane_off + kColO;
     const uint32_t tQ = tbase + lane_off + kColQ;
     const uint32_t tS0 = tbase + lane_off + kColS;
-    const float* my_row = reinterpret_cast<const float*>(smem + kXOff + r * kXRow * 4);
+    const uint8_t* my_row = smem + kXOff + r * 16;  // this head's 16 B of each token quad
     constexpr float kLn2 = 0.69314718055994530942f;
     int g = 0, seg_i = 0;
     bool ok = true;
@@ -630,10 +635,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  kSiteXchg, gi);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            const float* xin = my_row + xb * (kXBufBytes / 4);
+            const uint8_t* xin = my_row + xb * kXBufBytes;
 #pragma unroll
             for (int c = 0; c < kHalf; c += 4) {
-              const float4 pv = *reinterpret_cast<const float4*>(xin + c);
+              const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
               px[h * 32 + c] = pv.x; px[h * 32 + c + 1] = pv.y;
               px[h * 32 + c + 2] = pv.z; px[h * 32 + c + 3] = pv.w;
             }

@@ -212,6 +212,19 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
       : "memory");
 }
 
+// Bulk copy of `bytes` from this CTA's shared memory at `src` to the
+// shared::cluster address `dst` of another CTA of the cluster, completing the
+// bytes on the barrier at shared::cluster address `mbar` (in the destination
+// CTA).  Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
