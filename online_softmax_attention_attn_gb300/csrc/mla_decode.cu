@@ -24,8 +24,10 @@
 //     warps add the two partials in the same order on both CTAs and run the
 //     identical softmax; each CTA accumulates its 256 columns of O = P V in
 //     TMEM (V is the same shared-memory bytes as K).
-//   * Each 64-token page is one step (S MMAs with N=64) through a 3-stage TMA
-//     ring; the block table is read on the device and bounds-checked.  Two S
+//   * Each 64-token page is one step (S MMAs with N=64) through a 4-stage TMA
+//     ring of the CTA's c_kv atoms (rank 0's RoPE atom has a 2-slot ring of its
+//     own, freed as soon as S completes); the block table is read on the
+//     device and bounds-checked.  Two S
 //     buffers in TMEM let the tensor core compute step g+1 while the softmax
 //     of step g runs; the partial S travels in two 32-token halves.  Warps:
 //     0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer, 6-9 partial-S
@@ -53,11 +55,13 @@ constexpr int kPage = 64;
 constexpr int kStep = 64;                 // tokens per MMA step (one page)
 constexpr int kHalf = 32;                 // tokens per partial-S exchange
 constexpr int kThreads = 320;             // softmax, producer, MMA, exchange warps
-constexpr int kMaxAtoms = 5;              // 64-column atoms per CTA (rank 0)
 constexpr int kQAtomBytes = kHq * 128;    // 128 heads x 64 bf16
 constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
-constexpr int kStageBytes = kMaxAtoms * kKAtomBytes;  // 40 KB
-constexpr int kStages = 3;
+constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
+constexpr int kStages = 4;
+// Rank 0's RoPE atom of a step is read by the S MMAs only, so it has a ring
+// of its own that is released when S completes (much earlier than PV).
+constexpr int kRopeSlots = 2;
 constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
 // A received half is [token quad q][head][4 tokens] fp32: 16 B per head and
@@ -70,12 +74,14 @@ constexpr uint32_t kXBytes = kXBufBytes;       // payload per half step
 constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kQropeOff = 0;             // rank 0: q's RoPE atom (A of 4 S MMAs)
-constexpr int kStageOff = kQropeOff + kQAtomBytes;
+constexpr int kRopeOff = kQropeOff + kQAtomBytes;  // rank 0: k_rope ring
+constexpr int kStageOff = kRopeOff + kRopeSlots * kKAtomBytes;
 constexpr int kXOff = kStageOff + kStages * kStageBytes;
 constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
 // barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], s_read[2],
-// xfull[4], b_read[2], q_full, q_free, pv_done, o_free, mma_drain, o_ready
-constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6;
+// xfull[4], b_read[2], q_full, q_free, pv_done, o_free, mma_drain, o_ready,
+// rope_empty[2]
+constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6 + kRopeSlots;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -298,6 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   const uint32_t sQrope = base + kQropeOff;
+  const uint32_t sRope = base + kRopeOff;
   const uint32_t sStage = base + kStageOff;
   const uint32_t sX = base + kXOff;
   const uint32_t bar0 = base + kBarOff;
@@ -317,6 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // epilogue waits on it (pv_done completes once per step and may lag by more
   // than one phase at that point, so its parity would be ambiguous there).
   const uint32_t bar_o_ready = bar_q_full + 40;
+  auto bar_rope_empty = [&](int r) { return bar_q_full + 48 + 8u * r; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -340,6 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_o_free, 128);
     mbar_init(bar_mma_drain, 1);
     mbar_init(bar_o_ready, 1);
+    for (int r = 0; r < kRopeSlots; ++r) mbar_init(bar_rope_empty(r), 1);
     *abort_flag = 0;
     fence_mbar_init();
     // arm the receive barriers for half steps 0..3 (re-armed after each use)
@@ -375,6 +384,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
               if (!ok) break;
             }
+            const int rslot = g % kRopeSlots, ruse = g / kRopeSlots;
+            if (natoms == 5 && ruse > 0) {
+              ok = mbar_wait(bar_rope_empty(rslot), (ruse - 1) & 1, abort_flag, err, kSiteKvEmpty,
+                             g);
+              if (!ok) break;
+            }
             int blk = block_table[(size_t)s.b * max_blocks + t / kPage];
             if (blk < 0 || blk >= num_blocks) {
               record_error(err, ATTN_ERR_BAD_BLOCK_TABLE, s.b, t / kPage);
@@ -382,10 +397,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const int row = blk * kPage + (t % kPage);
             const uint32_t dst = sStage + slot * kStageBytes;
+            // the c_kv atoms into the stage and (rank 0) the RoPE atom into
+            // its own ring, all counted on the stage's full barrier
             mbar_arrive_expect_tx(bar_kv_full(slot), natoms * kKAtomBytes);
-            for (int a = 0; a < natoms; ++a)
+            for (int a = 0; a < 4; ++a)
               tma_load_2d_hint(dst + a * kKAtomBytes, &tmKV, bar_kv_full(slot), atom_col(a), row,
                                pol_kv);
+            if (natoms == 5)
+              tma_load_2d_hint(sRope + rslot * kKAtomBytes, &tmKV, bar_kv_full(slot), atom_col(4),
+                               row, pol_kv);
             issued = g + 1;
           }
         }
@@ -410,6 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // (the 14-bit address field never carries into the other fields).
       const uint64_t kdesc0 = sdesc_sw128(sStage, 16, 1024);
       const uint64_t qrdesc = sdesc_sw128(sQrope, 16, 1024);
+      const uint64_t kropedesc0 = sdesc_sw128(sRope, 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(sStage, kKAtomBytes, 1024);
       int g = 0, seg_i = 0;
       bool ok = true;
@@ -429,12 +450,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    kIdescS, (a | kk) != 0);
         }
         if (natoms == 5) {
+          const uint64_t rd = kropedesc0 + (uint64_t)(((gg % kRopeSlots) * kKAtomBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4),
-                   kd + (uint64_t)((4 * kKAtomBytes + kk * 32) >> 4), kIdescS, 1u);
+            mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
+                   kIdescS, 1u);
         }
         tc_commit(bar_s_full(gg % kSBufs));
+        if (natoms == 5) tc_commit(bar_rope_empty(gg % kRopeSlots));  // the RoPE slot is free
         return true;
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
