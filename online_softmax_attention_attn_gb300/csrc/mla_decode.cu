@@ -648,78 +648,135 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n && ok; ++i) {
           const int gi = g + i;
           const int sb = gi % kSBufs;
-          // peer's partial of step gi, two 32-token halves (pushed by its
-          // exchange warps)
-          float px[kStep];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          const int nvalid = L - (t0 + i * kStep);
+          const bool full = nvalid >= kStep;
+          // waits for the peer's half h and for this CTA's own partial
+          auto wait_peer = [&](int h) -> bool {
             const int xb = (2 * gi + h) % kXBufs;
-            ok = mbar_wait<true>(bar_xfull(xb), ((2 * gi + h) / kXBufs) & 1, abort_flag, err,
-                                 kSiteXchg, gi);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const uint8_t* xin = my_row + xb * kXBufBytes;
+            const bool w = mbar_wait<true>(bar_xfull(xb), ((2 * gi + h) / kXBufs) & 1,
+                                           abort_flag, err, kSiteXchg, gi);
+            return __all_sync(0xffffffffu, w);
+          };
+          bool s_seen = false;
+          auto wait_own = [&]() -> bool {
+            if (s_seen) return true;
+            const bool w = __all_sync(0xffffffffu, mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1,
+                                                             abort_flag, err, kSiteSFull, gi));
+            if (w) tc_fence_after();
+            s_seen = w;
+            return w;
+          };
+          uint32_t p[kStep / 2];
+          float alpha = 1.f;
+          bool resc = false;
+          bool done = false;
+          // Fast path (whole page visible, reference set, scale >= 0): each
+          // 32-token half is summed (own + peer partial: one rounding, the
+          // same bits on both CTAs) and turned into P = 2^(scale*s - m_ref)
+          // with the CURRENT reference as soon as it has arrived; kept while
+          // every row sum is at most 2^16 (which bounds every P).  Otherwise
+          // the slow path below redoes the step from the exact row max.
+          if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
+            float rr[8];
 #pragma unroll
-            for (int c = 0; c < kHalf; c += 4) {
-              const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
-              px[h * 32 + c] = pv.x; px[h * 32 + c + 1] = pv.y;
-              px[h * 32 + c + 2] = pv.z; px[h * 32 + c + 3] = pv.w;
+            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+            const float nm = -m_ref;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              ok = wait_peer(h) && wait_own();
+              if (!ok) break;
+              float sh[kHalf];
+              tmem_ld32(tS0 + sb * 64 + h * 32, sh);
+              const uint8_t* xin = my_row + ((2 * gi + h) % kXBufs) * kXBufBytes;
+#pragma unroll
+              for (int c = 0; c < kHalf; c += 8) {
+                const float4 qa = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
+                const float4 qb = *reinterpret_cast<const float4*>(xin + (c / 4 + 1) * kXQuadBytes);
+                const float pxv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                float tv[8], pv[8];
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                  float s0, s1;
+                  ffma2(s0, s1, sh[c + u], sh[c + u + 1], 1.f, 1.f, pxv[u], pxv[u + 1]);
+                  ffma2(tv[u], tv[u + 1], s0, s1, scale_log2, scale_log2, nm, nm);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2)
+                  p[(h * kHalf + c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+              }
+            }
+            if (!ok) break;
+            const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+            if (__all_sync(0xffffffffu, rs <= 65536.f)) {
+              l += rs;
+              done = true;
             }
           }
-          if (!ok) break;
-          mbar_arrive(bar_b_read(sb));  // the loads above have returned their values
-          // Re-arm both half-buffers for step gi + 2.  The peer can only send
-          // that step after this CTA has sent step gi + 1, which waits for
-          // every thread's b_read of this step.
+          if (!done) {
+            // slow path: the whole step (masked) from its exact row max
+            ok = wait_peer(0) && wait_peer(1) && wait_own();
+            if (!ok) break;
+            float px[kStep];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint8_t* xin = my_row + ((2 * gi + h) % kXBufs) * kXBufBytes;
+#pragma unroll
+              for (int c = 0; c < kHalf; c += 4) {
+                const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
+                px[h * 32 + c] = pv.x; px[h * 32 + c + 1] = pv.y;
+                px[h * 32 + c + 2] = pv.z; px[h * 32 + c + 3] = pv.w;
+              }
+            }
+            float sv[kStep];
+            tmem_ld64(tS0 + sb * 64, sv);
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kStep; c += 4) {
+              float t4[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float sum = sv[c + u] + px[c + u];
+                t4[u] = (c + u < nvalid) ? sum * scale_log2 : -INFINITY;
+                sv[c + u] = t4[u];
+              }
+              mx0 = fmaxf(mx0, t4[0]); mx1 = fmaxf(mx1, t4[1]);
+              mx2 = fmaxf(mx2, t4[2]); mx3 = fmaxf(mx3, t4[3]);
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const float m_new = fmaxf(m_ref, mt);
+            resc = m_new > m_ref + kRescaleThreshold;
+            if (resc) {
+              alpha = fast_exp2(m_ref - m_new);
+              m_ref = m_new;
+              l *= alpha;
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < kStep; c += 4) {
+              const float p0 = fast_exp2(sv[c] - m_use);
+              const float p1 = fast_exp2(sv[c + 1] - m_use);
+              const float p2 = fast_exp2(sv[c + 2] - m_use);
+              const float p3 = fast_exp2(sv[c + 3] - m_use);
+              rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
+              p[c / 2] = pack_bf16x2(p0, p1);
+              p[c / 2 + 1] = pack_bf16x2(p2, p3);
+            }
+            l += (rs0 + rs1) + (rs2 + rs3);
+          }
+          // Every read of the peer's partial of this step has returned: re-arm
+          // both half-buffers for step gi + 2 (the peer sends that step only
+          // after this CTA has sent step gi + 1, which waits for every thread's
+          // b_read of this step), then release them.
           if (r == 0) {
             mbar_arrive_expect_tx(bar_xfull((2 * gi) % kXBufs), kXBytes);
             mbar_arrive_expect_tx(bar_xfull((2 * gi + 1) % kXBufs), kXBytes);
           }
-          // own partial of step gi
-          ok = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull, gi);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-          float sv[kStep];
-          tmem_ld64(tS0 + sb * 64, sv);
-          // full S in the same summation order on both CTAs (rank 0 + rank 1)
-          const int nvalid = L - (t0 + i * kStep);
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < kStep; c += 4) {
-            float t4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float full = (rank == 0) ? (sv[c + u] + px[c + u]) : (px[c + u] + sv[c + u]);
-              t4[u] = (c + u < nvalid) ? full * scale_log2 : -INFINITY;
-              sv[c + u] = t4[u];
-            }
-            mx0 = fmaxf(mx0, t4[0]); mx1 = fmaxf(mx1, t4[1]);
-            mx2 = fmaxf(mx2, t4[2]); mx3 = fmaxf(mx3, t4[3]);
-          }
-          const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-          const float m_new = fmaxf(m_ref, mt);
-          const bool resc = m_new > m_ref + kRescaleThreshold;
-          float alpha = 1.f;
-          if (resc) {
-            alpha = fast_exp2(m_ref - m_new);
-            m_ref = m_new;
-            l *= alpha;
-          }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          uint32_t p[kStep / 2];
-          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-#pragma unroll
-          for (int c = 0; c < kStep; c += 4) {
-            const float p0 = fast_exp2(sv[c] - m_use);
-            const float p1 = fast_exp2(sv[c + 1] - m_use);
-            const float p2 = fast_exp2(sv[c + 2] - m_use);
-            const float p3 = fast_exp2(sv[c + 3] - m_use);
-            rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
-            p[c / 2] = pack_bf16x2(p0, p1);
-            p[c / 2 + 1] = pack_bf16x2(p2, p3);
-          }
-          l += (rs0 + rs1) + (rs2 + rs3);
+          mbar_arrive(bar_b_read(sb));
           // Tokens past the end contribute exactly zero even if the cache
           // tail holds non-finite bytes: clear those V rows before PV reads.
           // Each thread fences its own writes; the PV MMA is issued only after
