@@ -313,30 +313,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha = 1.f;
         bool resc = false;
         uint32_t p[32];
-        // Fast path (half fully visible, reference set, scale >= 0): P =
-        // 2^(scale*s - m_ref) with the CURRENT reference and no row max.  It
-        // is kept when every row sum of the half is at most kFastSumLimit,
-        // which bounds every P by that limit; otherwise S, still intact in
-        // TMEM, is reloaded and the half takes the slow path with its max.
+        // Fast path (reference set, scale >= 0): P = 2^(scale*s - m_ref) with
+        // the CURRENT reference and no row max.  It is kept when every row
+        // sum of the half is at most kFastSumLimit, which bounds every P by
+        // that limit; otherwise S, still intact in TMEM, is reloaded and the
+        // half takes the slow path with its exact max.
         bool done = false;
-        if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
+        if (__all_sync(0xffffffffu, m_ref != -INFINITY && scale_log2 >= 0.f)) {
           float sh[64], rr[8];
           const float nm = -m_ref;
 #pragma unroll
           for (int u = 0; u < 8; ++u) rr[u] = 0.f;
           tmem_ld64(tSh, sh);
+          // a half crossing the causal diagonal or the end of the keys gives
+          // its invisible keys P = 0 (the row-sum bound holds all the same)
+          if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            float tv[8], pv[8];
+            for (int c = 0; c < 64; c += 8) {
+              float tv[8], pv[8];
 #pragma unroll
-            for (int u = 0; u < 8; u += 2)
-              ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
+              for (int u = 0; u < 8; u += 2)
+                ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+              for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
 #pragma unroll
-            for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
 #pragma unroll
-            for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              float tv[8], pv[8];
+#pragma unroll
+              for (int u = 0; u < 8; u += 2)
+                ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) pv[u] = (c + u < nvalid) ? fast_exp2(tv[u]) : 0.f;
+#pragma unroll
+              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+            }
           }
           const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
           if (__all_sync(0xffffffffu, rs <= kFastSumLimit)) {
