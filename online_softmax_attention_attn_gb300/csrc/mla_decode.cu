@@ -15,7 +15,8 @@
 //     latent head (M=128, tcgen05 kind::f16, fp32 accumulators in TMEM).
 //   * O = 128 heads x 512 fp32 would fill all of one SM's TMEM, so a CLUSTER
 //     OF TWO CTAs shares each work item by columns: rank 0 owns latent
-//     columns [0,256) plus the 64 RoPE columns, rank 1 owns [256,512).  Each
+//     columns [0,256) and RoPE columns [512,544), rank 1 owns [256,512) and
+//     [544,576) (18 S MMAs each per step).  Each
 //     CTA TMA-loads only its own columns of every cached row (HBM is read
 //     once) and computes a partial S over them with its share of q held in
 //     TMEM.  Four exchange warps push each partial S tile into the peer's
@@ -59,9 +60,14 @@ constexpr int kQAtomBytes = kHq * 128;    // 128 heads x 64 bf16
 constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
 constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
 constexpr int kStages = 4;
-// Rank 0's RoPE atom of a step is read by the S MMAs only, so it has a ring
-// of its own that is released when S completes (much earlier than PV).
+// The 64 RoPE columns are split between the ranks, 32 each (64-byte rows,
+// 64-byte swizzle).  They are read by the S MMAs only, so they have a ring of
+// their own that is released when S completes (much earlier than PV).
 constexpr int kRopeSlots = 2;
+constexpr int kRopeCols = 32;                       // RoPE columns per CTA
+constexpr int kRopeRowBytes = kRopeCols * 2;        // 64 B
+constexpr int kQropeBytes = kHq * kRopeRowBytes;    // q's RoPE half: 8 KB
+constexpr int kKropeBytes = kStep * kRopeRowBytes;  // a step's k_rope half: 4 KB
 constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
 // A received half is [token quad q][head][4 tokens] fp32: 16 B per head and
@@ -73,9 +79,10 @@ constexpr int kXBufBytes = (kHalf / 4) * kXQuadBytes;
 constexpr uint32_t kXBytes = kXBufBytes;       // payload per half step
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kQropeOff = 0;             // rank 0: q's RoPE atom (A of 4 S MMAs)
-constexpr int kRopeOff = kQropeOff + kQAtomBytes;  // rank 0: k_rope ring
-constexpr int kStageOff = kRopeOff + kRopeSlots * kKAtomBytes;
+constexpr int kQropeOff = 0;             // q's RoPE half (A of 2 S MMAs)
+constexpr int kRopeOff = kQropeOff + kQropeBytes;  // k_rope ring
+constexpr int kStageOff = kRopeOff + kRopeSlots * kKropeBytes;
+static_assert(kStageOff % 1024 == 0, "swizzled stages start on 1024-byte boundaries");
 constexpr int kXOff = kStageOff + kStages * kStageBytes;
 constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
 // barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], s_read[2],
@@ -278,6 +285,7 @@ __device__ __forceinline__ int seg_steps(int p0, int p1, int L) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV,
+                      const __grid_constant__ CUtensorMap tmRope,
                       const __nv_bfloat16* __restrict__ q,
                       const int32_t* __restrict__ block_table,
                       const int32_t* __restrict__ seqlens, __nv_bfloat16* __restrict__ o,
@@ -297,11 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nchunks = hdr[1];
   if (cluster >= nchunks) return;  // both CTAs of the cluster leave together
 
-  // columns owned by this CTA, as 64-column atoms of the 576-wide row
-  const int natoms = rank == 0 ? 5 : 4;
-  auto atom_col = [&](int a) -> int {
-    return rank == 0 ? (a < 4 ? a * 64 : 512) : (256 + a * 64);
-  };
+  // columns owned by this CTA: four 64-column c_kv atoms of the 576-wide row
+  // and one half of the RoPE columns
+  auto atom_col = [&](int a) -> int { return (int)rank * 256 + a * 64; };
+  const int rope_col = 512 + (int)rank * kRopeCols;
 
   const uint32_t sQrope = base + kQropeOff;
   const uint32_t sRope = base + kRopeOff;
@@ -354,6 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // arm the receive barriers for half steps 0..3 (re-armed after each use)
     for (int b = 0; b < kXBufs; ++b) mbar_arrive_expect_tx(bar_xfull(b), kXBytes);
     prefetch_tmap(&tmKV);
+    prefetch_tmap(&tmRope);
   }
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -385,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (!ok) break;
             }
             const int rslot = g % kRopeSlots, ruse = g / kRopeSlots;
-            if (natoms == 5 && ruse > 0) {
+            if (ruse > 0) {
               ok = mbar_wait(bar_rope_empty(rslot), (ruse - 1) & 1, abort_flag, err, kSiteKvEmpty,
                              g);
               if (!ok) break;
@@ -397,15 +405,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const int row = blk * kPage + (t % kPage);
             const uint32_t dst = sStage + slot * kStageBytes;
-            // the c_kv atoms into the stage and (rank 0) the RoPE atom into
-            // its own ring, all counted on the stage's full barrier
-            mbar_arrive_expect_tx(bar_kv_full(slot), natoms * kKAtomBytes);
+            // the c_kv atoms into the stage and the RoPE half into its own
+            // ring, all counted on the stage's full barrier
+            mbar_arrive_expect_tx(bar_kv_full(slot), 4 * kKAtomBytes + kKropeBytes);
             for (int a = 0; a < 4; ++a)
               tma_load_2d_hint(dst + a * kKAtomBytes, &tmKV, bar_kv_full(slot), atom_col(a), row,
                                pol_kv);
-            if (natoms == 5)
-              tma_load_2d_hint(sRope + rslot * kKAtomBytes, &tmKV, bar_kv_full(slot), atom_col(4),
-                               row, pol_kv);
+            tma_load_2d_hint(sRope + rslot * kKropeBytes, &tmRope, bar_kv_full(slot), rope_col, row,
+                             pol_kv);
             issued = g + 1;
           }
         }
@@ -429,8 +436,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // Descriptors are built once; per MMA only the start address moves
       // (the 14-bit address field never carries into the other fields).
       const uint64_t kdesc0 = sdesc_sw128(sStage, 16, 1024);
-      const uint64_t qrdesc = sdesc_sw128(sQrope, 16, 1024);
-      const uint64_t kropedesc0 = sdesc_sw128(sRope, 16, 1024);
+      const uint64_t qrdesc = sdesc_sw64(sQrope, 512);
+      const uint64_t kropedesc0 = sdesc_sw64(sRope, 512);
       const uint64_t vdesc0 = sdesc_sw128(sStage, kKAtomBytes, 1024);
       int g = 0, seg_i = 0;
       bool ok = true;
@@ -442,22 +449,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t kd = kdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
         const uint32_t tS = tbase + kColS + (gg % kSBufs) * 64;
-        // c_kv atoms: q from TMEM; rank 0's RoPE atom: q from shared memory
+        // c_kv atoms: q from TMEM; the RoPE half: q from shared memory
         for (int a = 0; a < 4; ++a) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tS, tQ + a * 32 + kk * 8, kd + (uint64_t)((a * kKAtomBytes + kk * 32) >> 4),
                    kIdescS, (a | kk) != 0);
         }
-        if (natoms == 5) {
-          const uint64_t rd = kropedesc0 + (uint64_t)(((gg % kRopeSlots) * kKAtomBytes) >> 4);
+        {
+          const uint64_t rd = kropedesc0 + (uint64_t)(((gg % kRopeSlots) * kKropeBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < kRopeCols / 16; ++kk)
             mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
                    kIdescS, 1u);
         }
         tc_commit(bar_s_full(gg % kSBufs));
-        if (natoms == 5) tc_commit(bar_rope_empty(gg % kRopeSlots));  // the RoPE slot is free
+        tc_commit(bar_rope_empty(gg % kRopeSlots));  // the RoPE slot is free
         return true;
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
@@ -623,12 +630,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tmem_st32(tQ + a * 32, w);
           }
-          if (natoms == 5) {
-            // RoPE atom -> shared memory, 128-byte swizzled rows (K-major A)
-            uint8_t* qr = smem + kQropeOff + r * 128;
+          {
+            // RoPE half -> shared memory, 64-byte rows with the 64-byte
+            // swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3))
+            uint8_t* qr = smem + kQropeOff + r * kRopeRowBytes;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(qr + ((c ^ (r & 7)) * 16)) = __ldg(qrow + 512 / 8 + c);
+            for (int c = 0; c < kRopeRowBytes / 16; ++c)
+              *reinterpret_cast<uint4*>(qr + ((c ^ ((r >> 1) & 3)) * 16)) =
+                  __ldg(qrow + rope_col / 8 + c);
             fence_proxy_async_smem();
           }
           tmem_st_wait();
@@ -905,16 +914,21 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
   if (c0 == 0) lse[orow] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
 }
 
-CUresult make_map_2d(CUtensorMap* map, const void* ptr, long long rows, int box_rows) {
+// The latent pool as a 2-D tensor [rows, 576]: boxes of `box_cols` columns x
+// `box_rows` rows with 128-byte (64 columns) or 64-byte (32 columns) swizzle.
+CUresult make_map_2d(CUtensorMap* map, const void* ptr, long long rows, int box_rows,
+                     int box_cols) {
   PFN_encodeTiled enc = get_encode_tiled();
   if (!enc) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // Clusters of two that can be resident at once (cached per device).
@@ -966,8 +980,10 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   float* plse = reinterpret_cast<float*>(ws + w.plse);
   float* po = reinterpret_cast<float*>(ws + w.po);
 
-  CUtensorMap mkv;
-  CUresult r = make_map_2d(&mkv, a.kv, (long long)a.num_blocks * kPage, kStep);
+  CUtensorMap mkv, mrope;
+  CUresult r = make_map_2d(&mkv, a.kv, (long long)a.num_blocks * kPage, kStep, 64);
+  if (r == CUDA_SUCCESS)
+    r = make_map_2d(&mrope, a.kv, (long long)a.num_blocks * kPage, kStep, kRopeCols);
   if (r != CUDA_SUCCESS) {
     attn_set_error("mla_decode: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return cudaErrorInvalidValue;
@@ -978,7 +994,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   mla_decode_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(
-      mkv, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
+      mkv, mrope, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
       static_cast<__nv_bfloat16*>(a.o), a.lse, hdr, prefix, bounds, plse, po, a.B, a.max_blocks,
       a.num_blocks, scale_log2, a.err);
   e = cudaGetLastError();

@@ -64,7 +64,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank)
       : "memory");
 }
 
-// One non-blocking probe of the phase with parity `parity`.
+// One probe of the phase with parity `parity` (may suspend the thread briefly).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -77,7 +77,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same probe with cluster-scope acquire (for arrivals made by a peer CTA).
 // Non-blocking test of a phase: a cheaper first look than try_wait when the
 // phase has usually completed already.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
@@ -92,6 +91,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with cluster-scope acquire (for arrivals made by a peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -316,6 +316,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
   return (uint64_t)((saddr >> 4) & 0x3FFFu) |
          ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Shared-memory matrix descriptor, 64-byte swizzle, K-major operand: rows of
+// 64 B (32 bf16), 8-row groups `sbo` apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
 // 32 lanes x 64 columns of 32-bit TMEM -> registers, waited.
