@@ -152,6 +152,18 @@ def _sampled(cfg, n, seed):
     assert np.abs(o).max() <= float(kv.float().abs().max())
 
 
+def test_scores_jump_on_a_later_page():
+    """One late page scores far above the rest: the decode's per-half fast
+    path must fall back, move the reference and rescale O in TMEM."""
+    q, kv, table, sl = mla_inputs(3, 128, [1000, 640, 1500], seed=31)
+    q = (q.float() + 0.3).to(q.dtype)  # a component every head shares ...
+    for b in range(3):
+        page = int(table[b, 7])          # ... lifts page 7 by ~18 in log2 units
+        kv[page] = (kv[page].float() + 1.0).to(kv.dtype)
+    o, lse = _gpu(q, kv, table, sl)
+    _check(q, kv, table, sl, o, lse)
+
+
 def test_decode_batch64_workload_sampled():
     _sampled(MLA_B64, 192, 1)
 

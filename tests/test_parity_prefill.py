@@ -123,6 +123,27 @@ def test_bf16_long_rows_exercise_lazy_rescale():
     _check_full(q.bfloat16(), k.bfloat16(), v.bfloat16(), True, 0.5)
 
 
+def test_bf16_sudden_max_jump_inside_a_block():
+    """Keys 192..255 score far above everything before them: the second half of
+    KV block 1 moves the running reference, so O (holding block 0 and the
+    first half of block 1) is rescaled after that half's PV has landed."""
+    B, H, N, D = 1, 2, 512, 128
+    q, k, v = mha_inputs(B, H, N, D, torch.float32, seed=21)
+    q = q + 0.5                   # a component every query shares ...
+    k[:, :, 192:256, :] += 1.5    # ... lifts these keys by ~12 in log2 units
+    for causal in (False, True):
+        _check_full(q.bfloat16(), k.bfloat16(), v.bfloat16(), causal, 1.0 / math.sqrt(D))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.05])
+def test_bf16_zero_and_negative_scale(scale):
+    """A zero scale gives plain means; a negative one flips the max to a min:
+    both bypass the fast path's assumptions."""
+    q, k, v = mha_inputs(1, 2, 300, 128, torch.bfloat16, seed=23)
+    for causal in (False, True):
+        _check_full(q, k, v, causal, scale)
+
+
 def test_bf16_prefill_workload_sampled():
     cfg = BF16_PREFILL
     q, k, v = mha_config_inputs(cfg)
