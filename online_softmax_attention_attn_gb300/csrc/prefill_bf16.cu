@@ -11,17 +11,24 @@
 // suggests (fp32 -> bf16 conversion of P).
 //
 // How it maps onto GB300 (nothing here is taken from the pages' Ampere,
-// Hopper or RTX kernels).  One CTA owns TWO consecutive 128-row Q tiles of
-// one head and streams that head's K/V blocks once for both:
-//   * warp 8  : TMA producer.  Both Q tiles once, then K_j and V_j together
-//               into a ring of stages (128-byte swizzle), one full and one
-//               empty mbarrier per stage.
+// Hopper or RTX kernels).  A work item is TWO consecutive 128-row Q tiles of
+// one head, whose K/V blocks are streamed once for both.  The kernel is
+// persistent (one CTA per SM); each CTA runs items one after another:
+//   * warp 8  : TMA producer and work source.  Per item: each Q tile as soon
+//               as the previous item's last S MMA of that tile is done, then
+//               K_j and V_j together into a ring of stages (128-byte
+//               swizzle), one full and one empty mbarrier per stage.  The next
+//               item is claimed from the launch's ticket counter only after
+//               this item's last K/V load is issued, so items go to the CTAs
+//               that free up first; its number reaches the other warps
+//               through a 4-slot ring in shared memory.
 //   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
 //               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
 //               O_t += P_t V_j with P read straight from TMEM as the A operand,
 //               in two halves of 64 keys.  The issue order S0_0, S1_0, PV0_0,
 //               S0_1, PV1_0, S1_1, ... lets the tensor core work on one tile
-//               while the other tile's softmax runs (ping-pong).
+//               while the other tile's softmax runs (ping-pong).  Per-block
+//               barrier phases run on across items.
 //   * warps 0-3 / 4-7 : softmax warpgroup of tile 0 / tile 1, one thread per
 //               query row (TMEM lane = row).  Each block's 128 keys are taken
 //               as two online-softmax steps of 64 keys: load the S half, mask,
@@ -32,14 +39,20 @@
 //               is kept while every half-row sum is at most 2^16 (so every P
 //               is), otherwise the half is redone with its exact max.  O in
 //               TMEM is rescaled only when the max grew by more than 2^8 (lazy
-//               rescale; exact because O and l share the stale reference), and
-//               finally O/l -> bf16 -> smem -> TMA store, plus LSE.
+//               rescale; exact because O and l share the stale reference).
+//               The epilogue reads O_t out of TMEM (releasing it to the next
+//               item's first PV), then O/l -> bf16 one 64-column atom at a time
+//               through the tile's own 16 KB staging buffer -> TMA store, LSE.
 //   TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
-//   Work order: heads in groups of 16 (the CTAs running together share those
+//   Item order: heads in groups of 16 (the CTAs running together share those
 //   heads' K/V in L2), heaviest causal Q pairs first within a group.
 //   Every wait is bounded (about 2 s); a stuck pipeline records
 //   ATTN_ERR_DEVICE_TIMEOUT and the CTA unwinds, frees TMEM and exits.
 #include <math.h>
+
+#include <atomic>
+#include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -55,6 +68,7 @@ constexpr int kAtomBytes = 128 * 128; // one 128-row x 64-col bf16 swizzle colum
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kFastSumLimit = 65536.0f;   // fast path kept while every half-row sum <= 2^16
 constexpr int kHeadGroup = 16;             // heads scheduled together
+constexpr int kItemSlots = 4;              // work items handed from the producer to the others
 
 template <int D>
 struct Cfg {
@@ -64,17 +78,50 @@ struct Cfg {
   static constexpr int kStages = (D == 128) ? 2 : 5;      // ring slots (one KV block each)
   static constexpr int kQOff = 0;                          // Q0, Q1
   static constexpr int kRingOff = kTilesPerCta * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[tile], p_full[tile][half],
-  // pv_done[tile][half], mma_drain.  The per-half barriers each complete once
-  // per KV block, so no waiter is ever two phases behind or ahead of one.
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 4 + 4 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr int kOutOff = kRingOff + kStages * kStageBytes;  // O staging, one atom per tile
+  static constexpr int kBarOff = kOutOff + kTilesPerCta * kAtomBytes;
+  // barriers: q_full[tile], q_free[tile], kv_full[S], kv_empty[S], s_full[tile],
+  // p_full[tile][half], pv_done[tile][half], o_free[tile], item_full[4],
+  // item_empty[4], mma_drain.  The per-half barriers each complete once per
+  // KV block, so no waiter is ever two phases behind or ahead of one.
+  static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 4 + 4 + 2 + 2 * kItemSlots + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, item ring
+  static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // + 128 * tile
   static constexpr uint32_t kColO = 256;  // + 128 * tile
 };
+
+// A work item is a pair of consecutive Q tiles of one head.  Items are
+// numbered in heads of groups of kHeadGroup (the CTAs running together share
+// those heads' K/V in L2) and, within a group, heaviest causal pairs first.
+struct Item {
+  int bh, pr;
+  int T[kTilesPerCta];  // KV blocks visited by each Q tile (0: tile absent)
+};
+
+template <bool kCausal>
+__device__ __forceinline__ Item decode_item(int item, int BH, int N) {
+  const int n_qt = (N + kBM - 1) / kBM;
+  const int n_pairs = (n_qt + 1) / 2;
+  const int group = item / (kHeadGroup * n_pairs);
+  const int g_heads = min(kHeadGroup, BH - group * kHeadGroup);
+  const int rem = item - group * kHeadGroup * n_pairs;
+  Item it;
+  it.bh = group * kHeadGroup + rem % g_heads;
+  it.pr = kCausal ? (n_pairs - 1 - rem / g_heads) : (rem / g_heads);
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int qt = 2 * it.pr + t;
+    if (qt >= n_qt) {
+      it.T[t] = 0;
+    } else {
+      const int kv_limit = kCausal ? min(qt * kBM + kBM, N) : N;
+      it.T[t] = (kv_limit + kBN - 1) / kBN;
+    }
+  }
+  return it;
+}
 
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -82,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmO, float* __restrict__ lse,
-                        int BH, int N, float scale_log2, int* err, int debug_skip_load) {
+                        int BH, int N, float scale_log2, int* err, int* ticket, int debug_skip_load) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: swizzle atoms must start on a 1024-byte boundary.
@@ -93,55 +140,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = base + C::kQOff;
   const uint32_t sRing = base + C::kRingOff;
   const uint32_t bar0 = base + C::kBarOff;
-  const uint32_t bar_q_full = bar0;
-  auto bar_kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
-  auto bar_s_full = [&](int t) { return bar0 + 8u * (1 + 2 * C::kStages + t); };
-  auto bar_p_full = [&](int t, int h) { return bar0 + 8u * (3 + 2 * C::kStages + 2 * t + h); };
-  auto bar_pv_done = [&](int t, int h) { return bar0 + 8u * (7 + 2 * C::kStages + 2 * t + h); };
-  const uint32_t bar_mma_drain = bar0 + 8u * (11 + 2 * C::kStages);
+  auto bar_q_full = [&](int t) { return bar0 + 8u * t; };
+  auto bar_q_free = [&](int t) { return bar0 + 8u * (2 + t); };
+  auto bar_kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (4 + C::kStages + s); };
+  auto bar_s_full = [&](int t) { return bar0 + 8u * (4 + 2 * C::kStages + t); };
+  auto bar_p_full = [&](int t, int h) { return bar0 + 8u * (6 + 2 * C::kStages + 2 * t + h); };
+  auto bar_pv_done = [&](int t, int h) { return bar0 + 8u * (10 + 2 * C::kStages + 2 * t + h); };
+  auto bar_o_free = [&](int t) { return bar0 + 8u * (14 + 2 * C::kStages + t); };
+  auto bar_item_full = [&](int i) { return bar0 + 8u * (16 + 2 * C::kStages + i); };
+  auto bar_item_empty = [&](int i) {
+    return bar0 + 8u * (16 + 2 * C::kStages + kItemSlots + i);
+  };
+  const uint32_t bar_mma_drain = bar0 + 8u * (16 + 2 * C::kStages + 2 * kItemSlots);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item: heads in groups of kHeadGroup (their K/V stay in L2);
-  // within a group, heaviest causal Q pairs first across the group's heads.
   const int n_qt = (N + kBM - 1) / kBM;
-  const int n_pairs = (n_qt + 1) / 2;
-  const int group = blockIdx.x / (kHeadGroup * n_pairs);
-  const int g_heads = min(kHeadGroup, BH - group * kHeadGroup);
-  const int rem = blockIdx.x - group * kHeadGroup * n_pairs;
-  const int bh = group * kHeadGroup + rem % g_heads;
-  const int pr = kCausal ? (n_pairs - 1 - rem / g_heads) : (rem / g_heads);
-  int Tt[kTilesPerCta];  // KV blocks visited by each Q tile (0: tile absent)
-#pragma unroll
-  for (int t = 0; t < kTilesPerCta; ++t) {
-    const int qt = 2 * pr + t;
-    if (qt >= n_qt) {
-      Tt[t] = 0;
-    } else {
-      const int kv_limit = kCausal ? min(qt * kBM + kBM, N) : N;
-      Tt[t] = (kv_limit + kBN - 1) / kBN;
-    }
-  }
-  const int ntiles = Tt[1] > 0 ? 2 : 1;
-  const int Tmax = max(Tt[0], Tt[1]);
+  const int total_items = ((n_qt + 1) / 2) * BH;
 
   // ---- setup: barriers (thread 0), TMEM (warp 9)
   if (threadIdx.x == 0) {
-    mbar_init(bar_q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);
-    }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_q_full(t), 1);
+      mbar_init(bar_q_free(t), 1);
       mbar_init(bar_s_full(t), 1);
+      mbar_init(bar_o_free(t), 128);
       for (int h = 0; h < 2; ++h) {
         mbar_init(bar_p_full(t, h), 128);
         mbar_init(bar_pv_done(t, h), 1);
       }
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(bar_item_full(i), 1);
+      mbar_init(bar_item_empty(i), 1 + 256);  // the MMA thread and every softmax thread
     }
     mbar_init(bar_mma_drain, 1);
     *abort_flag = 0;
@@ -161,47 +200,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 8) {
-    // ================= TMA producer =================
+    // ================= TMA producer and work-item source =================
     if (lane == 0) {
       const uint64_t pol_kv = policy_evict_last();  // K/V are re-read by the head's other CTAs
-      mbar_arrive_expect_tx(bar_q_full, ntiles * C::kTileBytes);
-      for (int t = 0; t < ntiles; ++t)
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full, a * 64,
-                      (2 * pr + t) * kBM, bh);
-      int issued_until = 0;  // blocks [0, issued_until) were issued
       const int skip_block = debug_skip_load > 0 ? debug_skip_load / 2 : -1;  // test hook
+      int kv = 0;             // K/V blocks this CTA has loaded (ring position)
+      uint32_t skipped = 0;   // bit (kv % 32): that load was skipped by the test hook
+      int qn[2] = {0, 0};     // Q loads per tile
       bool ok = true;
-      for (int j = 0; j < Tmax && ok; ++j) {
-        const int slot = j % C::kStages;
-        const int use = j / C::kStages;
-        if (use > 0) {
-          ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, j);
+      int item = blockIdx.x;  // first item; later ones come from the launch's ticket
+      for (int k = 0; ok; ++k) {
+        const int slot = k % kItemSlots;
+        if (k >= kItemSlots) {
+          ok = mbar_wait(bar_item_empty(slot), (k / kItemSlots - 1) & 1, abort_flag, err,
+                         kSiteQFull, k);
           if (!ok) break;
         }
-        if (j == skip_block) continue;
-        // K_j and V_j land on one barrier
-        const uint32_t dst = sRing + slot * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_kv_full(slot), C::kStageBytes);
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d_hint(dst + a * kAtomBytes, &tmK, bar_kv_full(slot), a * 64, j * kBN, bh,
-                           pol_kv);
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(slot), a * 64,
-                           j * kBN, bh, pol_kv);
-        issued_until = j + 1;
+        item_ring[slot] = item < total_items ? item : -1;
+        mbar_arrive(bar_item_full(slot));
+        if (item >= total_items) break;
+        const Item it = decode_item<kCausal>(item, BH, N);
+        // Q_t of this item once the previous item's last S of that tile is done
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          if (it.T[t] == 0) continue;
+          if (qn[t] > 0) {
+            ok = mbar_wait(bar_q_free(t), (qn[t] - 1) & 1, abort_flag, err, kSiteQFull, k);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(bar_q_full(t), C::kTileBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full(t), a * 64,
+                        (2 * it.pr + t) * kBM, it.bh);
+          ++qn[t];
+        }
+        if (!ok) break;
+        const int Tmax = max(it.T[0], it.T[1]);
+        for (int j = 0; j < Tmax; ++j, ++kv) {
+          const int s = kv % C::kStages;
+          const int use = kv / C::kStages;
+          if (use > 0) {
+            ok = mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, j);
+            if (!ok) break;
+          }
+          if (j == skip_block) {
+            skipped |= 1u << (kv & 31);
+            continue;
+          }
+          skipped &= ~(1u << (kv & 31));
+          // K_j and V_j land on one barrier
+          const uint32_t dst = sRing + s * C::kStageBytes;
+          mbar_arrive_expect_tx(bar_kv_full(s), C::kStageBytes);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d_hint(dst + a * kAtomBytes, &tmK, bar_kv_full(s), a * 64, j * kBN, it.bh,
+                             pol_kv);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(s), a * 64,
+                             j * kBN, it.bh, pol_kv);
+        }
+        // The next item is claimed only now, two blocks before this one ends,
+        // so items go to the CTAs that free up first (as a launch of one CTA
+        // per item would place them).
+        if (ok) item = (int)gridDim.x + atomicAdd(ticket, 1);
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA unwinds.
-        const int first = issued_until > C::kStages ? issued_until - C::kStages : 0;
-        for (int j = first; j < issued_until; ++j) {
-          if (j == skip_block) continue;
+        const int first = kv > C::kStages ? kv - C::kStages : 0;
+        for (int x = first; x < kv; ++x) {
+          if (skipped & (1u << (x & 31))) continue;
           volatile int never = 0;
-          mbar_wait(bar_kv_full(j % C::kStages), (j / C::kStages) & 1, &never, nullptr,
-                    kSiteDrain, j);
+          mbar_wait(bar_kv_full(x % C::kStages), (x / C::kStages) & 1, &never, nullptr,
+                    kSiteDrain, x);
         }
-        volatile int never = 0;
-        mbar_wait(bar_q_full, 0, &never, nullptr, kSiteDrain, -1);
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          if (qn[t] == 0) continue;
+          volatile int never = 0;
+          mbar_wait(bar_q_full(t), (qn[t] - 1) & 1, &never, nullptr, kSiteDrain, -1);
+        }
       }
     }
     __syncwarp();
@@ -216,14 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(sRing, 16, 1024);
       const uint64_t vd0 = sdesc_sw128(sRing, kAtomBytes, 1024);
-      bool ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
-      tc_fence_after();
+      int kv = 0;                // ring position of the current item's block 0
+      int bc0 = 0, bc1 = 0;      // KV blocks each tile has been through (barrier phases)
+      int qn0 = 0, qn1 = 0;      // items each tile has been loaded for
+      int T0 = 0, T1 = 0;        // the current item's KV blocks per tile
+      int pb0 = 0, pb1 = 0;      // phase offsets of the tiles' per-block barriers
+      bool ok = true;
+      using Tile0 = std::integral_constant<int, 0>;
+      using Tile1 = std::integral_constant<int, 1>;
 
-      // S_t = Q_t K_j^T (its wait also covers V_j, which shares the stage)
-      auto issue_s = [&](int t, int j) -> bool {
-        const int slot = j % C::kStages;
-        if (!mbar_wait(bar_kv_full(slot), (j / C::kStages) & 1, abort_flag, err, kSiteKvFull,
-                       j))
+      // S_t = Q_t K_j^T (its wait also covers V_j, which shares the stage).
+      // The tile is a compile-time constant so that the issue path carries
+      // no per-tile selects: every instruction of this thread delays the pipe.
+      auto issue_s = [&](auto tile, int j) -> bool {
+        constexpr int t = decltype(tile)::value;
+        const int x = kv + j;
+        const int slot = x % C::kStages;
+        if (!mbar_wait(bar_kv_full(slot), (x / C::kStages) & 1, abort_flag, err, kSiteKvFull, j))
           return false;
         tc_fence_after();
         const uint64_t qb = qd0 + (uint64_t)(t * (C::kTileBytes >> 4));
@@ -240,15 +324,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_t += P_t V_j in two halves of 64 keys: the softmax of tile t hands
       // each half h of P_t over on p_full[t][h], and that half's MMAs are
       // committed to pv_done[t][h] (each completes once per block).
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int slot = j % C::kStages;
+      auto issue_pv = [&](auto tile, int j) -> bool {
+        constexpr int t = decltype(tile)::value;
+        const int x = kv + j;
+        const int slot = x % C::kStages;
+        const int ph = (j & 1) ^ (t ? pb1 : pb0);
         const uint64_t vb = vd0 + (uint64_t)((slot * C::kStageBytes + C::kTileBytes) >> 4);
         const uint32_t dO = tbase + C::kColO + t * 128;
         const uint32_t aP = tbase + C::kColS + t * 128;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(bar_p_full(t, h), j & 1, abort_flag, err, kSitePFull, 2 * j + h))
+          if (!mbar_wait(bar_p_full(t, h), ph, abort_flag, err, kSitePFull, 2 * j + h))
             return false;
           tc_fence_after();
 #pragma unroll
@@ -261,19 +348,95 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(bar_pv_done(t, h));
         }
         // the stage of block j is free once the last tile reading it is done
-        const int last_t = (j < Tt[1]) ? 1 : 0;
-        if (t == last_t) tc_commit(bar_kv_empty(slot));
+        if (t == 1 || j >= T1) tc_commit(bar_kv_empty(slot));
+        return true;
+      };
+      // the first PV of tile t in an item overwrites O_t: the previous
+      // item's epilogue must have read it
+      auto wait_o_free = [&](auto tile) -> bool {
+        constexpr int t = decltype(tile)::value;
+        const int qn = t ? qn1 : qn0;
+        if (qn == 0) return true;
+        if (!mbar_wait(bar_o_free(t), (qn - 1) & 1, abort_flag, err, kSitePvDone, qn))
+          return false;
+        tc_fence_after();
         return true;
       };
 
-      for (int t = 0; t < kTilesPerCta && ok; ++t)
-        if (Tt[t] > 0) ok = issue_s(t, 0);
-      for (int j = 0; j < Tmax && ok; ++j) {
-        for (int t = 0; t < kTilesPerCta && ok; ++t) {
-          if (j >= Tt[t]) continue;
-          ok = issue_pv(t, j);
-          if (ok && j + 1 < Tt[t]) ok = issue_s(t, j + 1);
+      for (int k = 0; ok; ++k) {
+        const int islot = k % kItemSlots;
+        ok = mbar_wait(bar_item_full(islot), (k / kItemSlots) & 1, abort_flag, err, kSiteQFull, k);
+        if (!ok) break;
+        const int item = item_ring[islot];
+        mbar_arrive(bar_item_empty(islot));
+        if (item < 0) break;
+        const Item it = decode_item<kCausal>(item, BH, N);
+        T0 = it.T[0];  // tile 0 is always present
+        T1 = it.T[1];
+        pb0 = bc0 & 1;
+        pb1 = bc1 & 1;
+        const int Tmax = max(T0, T1);
+        // block 0 of both tiles (Q waits, O hand-over from the last item)
+        ok = mbar_wait(bar_q_full(0), qn0 & 1, abort_flag, err, kSiteQFull, k);
+        if (ok) {
+          tc_fence_after();
+          ok = issue_s(Tile0{}, 0);
         }
+        if (ok && T1 > 0) {
+          ok = mbar_wait(bar_q_full(1), qn1 & 1, abort_flag, err, kSiteQFull, k);
+          if (ok) {
+            tc_fence_after();
+            ok = issue_s(Tile1{}, 0);
+          }
+        }
+        // q_free[t] is committed right after the tile's last S: the producer
+        // then loads the next item's Q_t while this item's tail still runs.
+        if (ok && T0 == 1) tc_commit(bar_q_free(0));
+        if (ok && T1 == 1) tc_commit(bar_q_free(1));
+        if (ok) ok = wait_o_free(Tile0{}) && issue_pv(Tile0{}, 0);
+        if (ok && T0 > 1) {
+          ok = issue_s(Tile0{}, 1);
+          if (ok && T0 == 2) tc_commit(bar_q_free(0));
+        }
+        if (ok && T1 > 0) ok = wait_o_free(Tile1{}) && issue_pv(Tile1{}, 0);
+        if (ok && T1 > 1) {
+          ok = issue_s(Tile1{}, 1);
+          if (ok && T1 == 2) tc_commit(bar_q_free(1));
+        }
+        // blocks 1.. : the steady part has no last S of either tile and so
+        // no conditions; the tail (at most three blocks) has them.
+        const int Tmin = T1 > 0 ? min(T0, T1) : T0;
+        const int j_tail = max(1, Tmin - 2);
+        int j = 1;
+        if (T1 > 0) {
+          for (; j < j_tail && ok; ++j) {
+            ok = issue_pv(Tile0{}, j);
+            if (ok) ok = issue_s(Tile0{}, j + 1);
+            if (ok) ok = issue_pv(Tile1{}, j);
+            if (ok) ok = issue_s(Tile1{}, j + 1);
+          }
+        }
+        for (; j < Tmax && ok; ++j) {
+          if (j < T0) {
+            ok = issue_pv(Tile0{}, j);
+            if (ok && j + 1 < T0) {
+              ok = issue_s(Tile0{}, j + 1);
+              if (ok && j + 2 == T0) tc_commit(bar_q_free(0));
+            }
+          }
+          if (ok && j < T1) {
+            ok = issue_pv(Tile1{}, j);
+            if (ok && j + 1 < T1) {
+              ok = issue_s(Tile1{}, j + 1);
+              if (ok && j + 2 == T1) tc_commit(bar_q_free(1));
+            }
+          }
+        }
+        kv += Tmax;
+        bc0 += T0;
+        bc1 += T1;
+        qn0 += 1;
+        qn1 += T1 > 0 ? 1 : 0;
       }
       // Every MMA this thread issued must be complete before TMEM is freed.
       tc_commit(bar_mma_drain);
@@ -284,217 +447,244 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================= softmax warpgroups (tile t = warp / 4) ==============
     const int t = warp >> 2;
-    const int T = Tt[t];
     const int r = threadIdx.x & 127;  // row within the Q tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + lane_off + C::kColS + t * 128;
     const uint32_t tO = tbase + lane_off + C::kColO + t * 128;
-    const int q0 = (2 * pr + t) * kBM;
-    const int row = q0 + r;
-    const int lim = kCausal ? min(N, row + 1) : N;  // keys [0, lim) are visible
-    float m_ref = -INFINITY;  // running max (log2 units), lazily updated
-    float l = 0.f;
-    bool ok = true;
+    const uint32_t stage_addr = base + C::kOutOff + t * kAtomBytes;  // this tile's O staging
+    uint8_t* stage = smem + C::kOutOff + t * kAtomBytes;
+    int bc = 0;  // KV blocks this tile has been through (barrier phases)
 
-    for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(bar_s_full(t), j & 1, abort_flag, err, kSiteSFull, j);
-      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
-      if (!ok) break;
-      tc_fence_after();
-      // Each 64-key half of the block is an online-softmax step of its own:
-      // its P is handed to the MMA thread as soon as it is written, so the PV
-      // MMAs of the first half run while the second half is computed.
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int nvalid = lim - j * kBN - h * 64;  // keys c < nvalid of this half are visible
-        const bool full = nvalid >= 64;
-        const uint32_t tSh = tS + h * 64;  // this half's 64 S columns
-        const uint32_t tPh = tS + h * 32;  // its P (bf16 pairs, over already-read S columns)
-        float alpha = 1.f;
-        bool resc = false;
-        uint32_t p[32];
-        // Fast path (reference set, scale >= 0): P = 2^(scale*s - m_ref) with
-        // the CURRENT reference and no row max.  It is kept when every row
-        // sum of the half is at most kFastSumLimit, which bounds every P by
-        // that limit; otherwise S, still intact in TMEM, is reloaded and the
-        // half takes the slow path with its exact max.
-        bool done = false;
-        if (__all_sync(0xffffffffu, m_ref != -INFINITY && scale_log2 >= 0.f)) {
-          float sh[64], rr[8];
-          const float nm = -m_ref;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) rr[u] = 0.f;
-          tmem_ld64(tSh, sh);
-          // a half crossing the causal diagonal or the end of the keys gives
-          // its invisible keys P = 0 (the row-sum bound holds all the same)
-          if (__all_sync(0xffffffffu, full)) {
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              float tv[8], pv[8];
-#pragma unroll
-              for (int u = 0; u < 8; u += 2)
-                ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              float tv[8], pv[8];
-#pragma unroll
-              for (int u = 0; u < 8; u += 2)
-                ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) pv[u] = (c + u < nvalid) ? fast_exp2(tv[u]) : 0.f;
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
-            }
-          }
-          const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
-          if (__all_sync(0xffffffffu, rs <= kFastSumLimit)) {
-            tmem_st32(tPh, p);
-            l += rs;
-            done = true;
-          }
-        }
-        if (!done) {
-          float sv[64];
-          tmem_ld64(tSh, sv);  // S of this half is intact (no P stored over it yet)
-          float mt;
-          if (full) {
-            // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
-            float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
-            if (scale_log2 >= 0.f) {
-#pragma unroll
-              for (int c = 4; c < 64; c += 4) {
-                a0 = fmaxf(a0, sv[c]); a1 = fmaxf(a1, sv[c + 1]);
-                a2 = fmaxf(a2, sv[c + 2]); a3 = fmaxf(a3, sv[c + 3]);
-              }
-              mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
-            } else {
-#pragma unroll
-              for (int c = 4; c < 64; c += 4) {
-                a0 = fminf(a0, sv[c]); a1 = fminf(a1, sv[c + 1]);
-                a2 = fminf(a2, sv[c + 2]); a3 = fminf(a3, sv[c + 3]);
-              }
-              mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
-            }
-          } else {
-            mt = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              sv[c] = (c < nvalid) ? sv[c] * scale_log2 : -INFINITY;
-              mt = fmaxf(mt, sv[c]);
-            }
-          }
-          const float m_new = fmaxf(m_ref, mt);
-          resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
-          if (resc) {
-            alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
-            m_ref = m_new;
-            l *= alpha;
-          }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-#pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            float p0, p1, p2, p3;
-            if (full) {
-              p0 = fast_exp2(fmaf(sv[c], scale_log2, -m_use));
-              p1 = fast_exp2(fmaf(sv[c + 1], scale_log2, -m_use));
-              p2 = fast_exp2(fmaf(sv[c + 2], scale_log2, -m_use));
-              p3 = fast_exp2(fmaf(sv[c + 3], scale_log2, -m_use));
-            } else {
-              p0 = fast_exp2(sv[c] - m_use);
-              p1 = fast_exp2(sv[c + 1] - m_use);
-              p2 = fast_exp2(sv[c + 2] - m_use);
-              p3 = fast_exp2(sv[c + 3] - m_use);
-            }
-            r0 += p0; r1 += p1; r2 += p2; r3 += p3;
-            p[c / 2] = pack_bf16x2(p0, p1);
-            p[c / 2 + 1] = pack_bf16x2(p2, p3);
-          }
-          tmem_st32(tPh, p);
-          l += (r0 + r1) + (r2 + r3);
-        }
+    for (int k = 0;; ++k) {
+      const int islot = k % kItemSlots;
+      bool got = mbar_wait(bar_item_full(islot), (k / kItemSlots) & 1, abort_flag, err,
+                           kSiteQFull, k);
+      got = __all_sync(0xffffffffu, got);
+      const int item = got ? item_ring[islot] : -1;
+      if (got) mbar_arrive(bar_item_empty(islot));
+      // the four warps take the item (or stop) together
+      if (named_barrier_any(1 + t, 128, item < 0)) break;
+      const Item it = decode_item<kCausal>(item, BH, N);
+      const int T = t ? it.T[1] : it.T[0];
+      if (T == 0) continue;
+      const int bh = it.bh;
+      const int q0 = (2 * it.pr + t) * kBM;
+      const int row = q0 + r;
+      const int lim = kCausal ? min(N, row + 1) : N;  // keys [0, lim) are visible
+      float m_ref = -INFINITY;  // running max (log2 units), lazily updated
+      float l = 0.f;
+      bool ok = true;
 
-        // Lazy correction of O before this half's PV: needed only if some row
-        // of this warp moved its reference, and only once every earlier PV of
-        // the tile has landed: the second half of block j-1 (h = 0) or the
-        // first half of block j (h = 1).
-        if ((j > 0 || h > 0) && __any_sync(0xffffffffu, resc)) {
-          ok = h == 0 ? mbar_wait(bar_pv_done(t, 1), (j - 1) & 1, abort_flag, err, kSitePvDone,
-                                  2 * j)
-                      : mbar_wait(bar_pv_done(t, 0), j & 1, abort_flag, err, kSitePvDone,
-                                  2 * j + 1);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float ov[32];
-            tmem_ld32(tO + c * 32, ov);
-            uint32_t ou[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
-            tmem_st32(tO + c * 32, ou);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar_p_full(t, h));
-      }
-      if (!ok) break;
-    }
-
-    if (T > 0) {
-      if (ok) ok = mbar_wait(bar_pv_done(t, 1), (T - 1) & 1, abort_flag, err, kSitePvDone, 2 * T);
-      ok = __all_sync(0xffffffffu, ok);
-      const uint32_t stage_addr = sQ + t * C::kTileBytes;  // Q_t is no longer read
-      if (ok) {
+      for (int j = 0; j < T; ++j) {
+        ok = mbar_wait(bar_s_full(t), (bc + j) & 1, abort_flag, err, kSiteSFull, j);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+        if (!ok) break;
         tc_fence_after();
-        // ---- epilogue: O / l -> bf16 into the Q_t buffer, then TMA store
-        const float inv_l = 1.0f / l;
-        uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+        // Each 64-key half of the block is an online-softmax step of its own:
+        // its P is handed to the MMA thread as soon as it is written, so the PV
+        // MMAs of the first half run while the second half is computed.
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          const int atom = (c * 32) / 64;
-          const int chunk0 = ((c * 32) % 64) / 8;  // 16-byte chunk within the 128-B row
+        for (int h = 0; h < 2; ++h) {
+          const int nvalid = lim - j * kBN - h * 64;  // keys c < nvalid of this half are visible
+          const bool full = nvalid >= 64;
+          const uint32_t tSh = tS + h * 64;  // this half's 64 S columns
+          const uint32_t tPh = tS + h * 32;  // its P (bf16 pairs, over already-read S columns)
+          float alpha = 1.f;
+          bool resc = false;
+          uint32_t p[32];
+          // Fast path (reference set, scale >= 0): P = 2^(scale*s - m_ref) with
+          // the CURRENT reference and no row max.  It is kept when every row
+          // sum of the half is at most kFastSumLimit, which bounds every P by
+          // that limit; otherwise S, still intact in TMEM, is reloaded and the
+          // half takes the slow path with its exact max.
+          bool done = false;
+          if (__all_sync(0xffffffffu, m_ref != -INFINITY && scale_log2 >= 0.f)) {
+            float sh[64], rr[8];
+            const float nm = -m_ref;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
-            w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
-            w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
-            w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
-            const int phys = (chunk0 + q4) ^ (r & 7);  // 128-byte swizzle
-            *reinterpret_cast<uint4*>(stage + atom * kAtomBytes + r * 128 + phys * 16) = w;
+            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+            tmem_ld64(tSh, sh);
+            // a half crossing the causal diagonal or the end of the keys gives
+            // its invisible keys P = 0 (the row-sum bound holds all the same)
+            if (__all_sync(0xffffffffu, full)) {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8) {
+                float tv[8], pv[8];
+#pragma unroll
+                for (int u = 0; u < 8; u += 2)
+                  ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8) {
+                float tv[8], pv[8];
+#pragma unroll
+                for (int u = 0; u < 8; u += 2)
+                  ffma2(tv[u], tv[u + 1], sh[c + u], sh[c + u + 1], scale_log2, scale_log2, nm, nm);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pv[u] = (c + u < nvalid) ? fast_exp2(tv[u]) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+              }
+            }
+            const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+            if (__all_sync(0xffffffffu, rs <= kFastSumLimit)) {
+              tmem_st32(tPh, p);
+              l += rs;
+              done = true;
+            }
           }
+          if (!done) {
+            float sv[64];
+            tmem_ld64(tSh, sv);  // S of this half is intact (no P stored over it yet)
+            float mt;
+            if (full) {
+              // max of scale*s is scale*max(s) (or scale*min(s) for a negative scale)
+              float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
+              if (scale_log2 >= 0.f) {
+#pragma unroll
+                for (int c = 4; c < 64; c += 4) {
+                  a0 = fmaxf(a0, sv[c]); a1 = fmaxf(a1, sv[c + 1]);
+                  a2 = fmaxf(a2, sv[c + 2]); a3 = fmaxf(a3, sv[c + 3]);
+                }
+                mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+              } else {
+#pragma unroll
+                for (int c = 4; c < 64; c += 4) {
+                  a0 = fminf(a0, sv[c]); a1 = fminf(a1, sv[c + 1]);
+                  a2 = fminf(a2, sv[c + 2]); a3 = fminf(a3, sv[c + 3]);
+                }
+                mt = fminf(fminf(a0, a1), fminf(a2, a3)) * scale_log2;
+              }
+            } else {
+              mt = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                sv[c] = (c < nvalid) ? sv[c] * scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sv[c]);
+              }
+            }
+            const float m_new = fmaxf(m_ref, mt);
+            resc = m_new > m_ref + kRescaleThreshold;  // false while both -inf
+            if (resc) {
+              alpha = fast_exp2(m_ref - m_new);  // 0 when m_ref == -inf
+              m_ref = m_new;
+              l *= alpha;
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              float p0, p1, p2, p3;
+              if (full) {
+                p0 = fast_exp2(fmaf(sv[c], scale_log2, -m_use));
+                p1 = fast_exp2(fmaf(sv[c + 1], scale_log2, -m_use));
+                p2 = fast_exp2(fmaf(sv[c + 2], scale_log2, -m_use));
+                p3 = fast_exp2(fmaf(sv[c + 3], scale_log2, -m_use));
+              } else {
+                p0 = fast_exp2(sv[c] - m_use);
+                p1 = fast_exp2(sv[c + 1] - m_use);
+                p2 = fast_exp2(sv[c + 2] - m_use);
+                p3 = fast_exp2(sv[c + 3] - m_use);
+              }
+              r0 += p0; r1 += p1; r2 += p2; r3 += p3;
+              p[c / 2] = pack_bf16x2(p0, p1);
+              p[c / 2 + 1] = pack_bf16x2(p2, p3);
+            }
+            tmem_st32(tPh, p);
+            l += (r0 + r1) + (r2 + r3);
+          }
+
+          // Lazy correction of O before this half's PV: needed only if some row
+          // of this warp moved its reference, and only once every earlier PV of
+          // the tile has landed: the second half of block j-1 (h = 0) or the
+          // first half of block j (h = 1).
+          if ((j > 0 || h > 0) && __any_sync(0xffffffffu, resc)) {
+            ok = h == 0 ? mbar_wait(bar_pv_done(t, 1), (bc + j - 1) & 1, abort_flag, err,
+                                    kSitePvDone, 2 * j)
+                        : mbar_wait(bar_pv_done(t, 0), (bc + j) & 1, abort_flag, err, kSitePvDone,
+                                    2 * j + 1);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              float ov[32];
+              tmem_ld32(tO + c * 32, ov);
+              uint32_t ou[32];
+#pragma unroll
+              for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
+              tmem_st32(tO + c * 32, ou);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_p_full(t, h));
         }
-        fence_proxy_async_smem();
-        if (row < N) {
-          constexpr float kLn2 = 0.69314718055994530942f;
-          lse[(size_t)bh * N + row] = (m_ref + log2f(l)) * kLn2;
+
+        if (!ok) break;
+      }
+
+      // ---- epilogue: O / l -> bf16, one 64-column atom at a time through this
+      // tile's staging buffer, each stored by TMA; LSE.  All four warps of the
+      // warpgroup reach every barrier below on every path (their waits are
+      // bounded); stores are skipped once any role has aborted.
+      if (ok) ok = mbar_wait(bar_pv_done(t, 1), (bc + T - 1) & 1, abort_flag, err, kSitePvDone, 2 * T);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after();
+      const float inv_l = 1.0f / l;
+#pragma unroll 1
+      for (int a = 0; a < C::kAtoms; ++a) {
+        // the previous store from the staging buffer has read it
+        if (r == 0) bulk_wait_all_read();
+        named_barrier_sync(1 + t, 128);
+        if (ok) {
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            float ov[32];
+            tmem_ld32(tO + a * 64 + c * 32, ov);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
+              w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
+              w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
+              w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
+              const int phys = (c * 4 + q4) ^ (r & 7);  // 128-byte swizzle
+              *reinterpret_cast<uint4*>(stage + r * 128 + phys * 16) = w;
+            }
+          }
+          if (a == C::kAtoms - 1) {
+            // O_t is read: the next item's first PV of this tile may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar_o_free(t));
+          }
+          fence_proxy_async_smem();
         }
+        const bool stop = named_barrier_any(1 + t, 128, !ok || *abort_flag != 0);
+        if (r == 0 && !stop) {
+          tma_store_3d(&tmO, stage_addr, a * 64, q0, bh);
+          bulk_commit();
+        }
+        ok = ok && !stop;
       }
-      // All four warps of this warpgroup reach this barrier on every path
-      // (their waits are bounded); the store is skipped if any role aborted.
-      named_barrier_sync(1 + t, 128);
-      if (r == 0 && *abort_flag == 0) {
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_store_3d(&tmO, stage_addr + a * kAtomBytes, a * 64, q0, bh);
-        bulk_commit();
-        bulk_wait_all();
+      if (ok && row < N) {
+        constexpr float kLn2 = 0.69314718055994530942f;
+        lse[(size_t)bh * N + row] = (m_ref + log2f(l)) * kLn2;
       }
+      bc += T;
+      // one decision for the whole warpgroup: go on to the next item or stop
+      if (named_barrier_any(1 + t, 128, !ok || *abort_flag != 0)) break;
     }
+    if (r == 0) bulk_wait_all();  // this tile's O stores are complete
   }
 
   // ---- teardown: every role has finished (or unwound); free TMEM
@@ -518,9 +708,41 @@ CUresult make_map_3d(CUtensorMap* map, const void* ptr, int D, int N, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-long long num_ctas(int B, int H, int N) {
+long long num_items(int B, int H, int N) {
   const int n_qt = (N + kBM - 1) / kBM;
   return (long long)((n_qt + 1) / 2) * B * H;
+}
+
+// Work-item tickets: each launch takes one counter (round robin over
+// kTicketSlots), zeroes it on its stream, and its CTAs draw items from it.
+// A slot is reused kTicketSlots launches later, by which time a launch on the
+// same stream has finished; launches in flight at once on different streams
+// need distinct slots, so up to kTicketSlots of them may overlap.
+constexpr int kTicketSlots = 64;
+__device__ int g_prefill_tickets[kTicketSlots];
+std::atomic<unsigned> g_ticket_next{0};
+void* g_ticket_base[64] = {};
+std::mutex g_ticket_mu;
+
+cudaError_t ticket_for_launch(cudaStream_t s, int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* basep = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ticket_mu);
+    if (g_ticket_base[dev] == nullptr) {
+      e = cudaGetSymbolAddress(&g_ticket_base[dev], g_prefill_tickets);
+      if (e != cudaSuccess) return e;
+    }
+    basep = g_ticket_base[dev];
+  }
+  int* slot = static_cast<int*>(basep) + (g_ticket_next.fetch_add(1) % kTicketSlots);
+  e = cudaMemsetAsync(slot, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  *out = slot;
+  return cudaSuccess;
 }
 
 template <int D, bool kCausal>
@@ -532,8 +754,14 @@ cudaError_t launch_t(const PrefillBf16Args& a, const CUtensorMap& mq, const CUte
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<(unsigned)num_ctas(a.B, a.H, a.N), kThreads, C::kSmemBytes, s>>>(
-      mq, mk, mv, mo, a.lse, a.B * a.H, a.N, scale_log2, a.err, a.debug_skip_load);
+  int* ticket = nullptr;
+  e = ticket_for_launch(s, &ticket);
+  if (e != cudaSuccess) return e;
+  // persistent: one CTA per SM (the shared memory allows no more)
+  const long long items = num_items(a.B, a.H, a.N);
+  const unsigned grid = (unsigned)(items < a.num_sms ? items : a.num_sms);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, mo, a.lse, a.B * a.H, a.N, scale_log2,
+                                              a.err, ticket, a.debug_skip_load);
   return cudaGetLastError();
 }
 
@@ -552,8 +780,8 @@ bool prefill_bf16_info(int D, int* Br, int* Bc, int* threads, int* smem) {
 }
 
 cudaError_t launch_prefill_bf16(const PrefillBf16Args& a, cudaStream_t s) {
-  const long long blocks = num_ctas(a.B, a.H, a.N);
-  if (blocks > 0x7fffffffLL) {
+  const long long blocks = num_items(a.B, a.H, a.N);
+  if (blocks > 0x7fffffffLL / 2) {
     attn_set_error("attn_fwd: too many query blocks (%lld)", blocks);
     return cudaErrorInvalidValue;
   }

@@ -156,3 +156,52 @@ def test_bf16_repeat_calls_are_bitwise_identical():
     a = _run(q, k, v, True, 0.09)
     b = _run(q, k, v, True, 0.09)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ persistent schedule
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_many_items_per_cta(causal):
+    """192 heads x 2 Q-tile pairs = 384 work items on ~150 persistent CTAs; the
+    second pair of every head has no second tile (N = 3 tiles of 128)."""
+    B, H, N, D = 4, 48, 384, 128
+    q, k, v = mha_inputs(B, H, N, D, torch.bfloat16, seed=31 + int(causal))
+    o, lse = _run(q, k, v, causal, 1.0 / math.sqrt(D))
+    _check_sampled(q, k, v, causal, 1.0 / math.sqrt(D), o, lse, nrows=768, seed=7)
+
+
+def test_bf16_more_launches_than_ticket_slots():
+    """Each launch draws its items from one of a fixed set of counters; many
+    launches in a row reuse them and every result stays the same."""
+    q, k, v = mha_inputs(2, 8, 640, 128, torch.bfloat16, seed=41)
+    dev = torch.device("cuda")
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    o0, l0 = pkg.attn_fwd(dq, dk, dv, causal=True, scale=0.1)
+    o, l = torch.empty_like(o0), torch.empty_like(l0)
+    for _ in range(150):
+        pkg.attn_fwd(dq, dk, dv, o, l, causal=True, scale=0.1)
+    pkg.attn_device_status()
+    assert torch.equal(o, o0) and torch.equal(l, l0)
+    ro, rl = oracle.mha(q, k, v, True, 0.1, rows=np.arange(0, 2 * 8 * 640, 97))
+    assert np.abs(o0.float().cpu().numpy().reshape(-1, 128)[::97] - ro).max() <= 2e-2
+    assert np.abs(l0.cpu().numpy().reshape(-1)[::97] - rl).max() <= 1e-3
+
+
+def test_bf16_two_streams_at_once():
+    """Launches on two streams may run together; each has its own counter."""
+    dev = torch.device("cuda")
+    qa, ka, va = (t.to(dev) for t in mha_inputs(2, 16, 1024, 128, torch.bfloat16, seed=43))
+    qb, kb, vb = (t.to(dev) for t in mha_inputs(2, 16, 1024, 128, torch.bfloat16, seed=44))
+    ra = pkg.attn_fwd(qa, ka, va, causal=True)
+    rb = pkg.attn_fwd(qb, kb, vb, causal=False)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(5):
+        with torch.cuda.stream(sa):
+            oa = pkg.attn_fwd(qa, ka, va, causal=True)
+        with torch.cuda.stream(sb):
+            ob = pkg.attn_fwd(qb, kb, vb, causal=False)
+        torch.cuda.synchronize()
+        pkg.attn_device_status()
+        assert torch.equal(oa[0], ra[0]) and torch.equal(oa[1], ra[1])
+        assert torch.equal(ob[0], rb[0]) and torch.equal(ob[1], rb[1])
