@@ -78,6 +78,12 @@ extern "C" {
  *   stream  : cudaStream_t or NULL.
  * Requirements: all pointers non-null and 16-byte aligned; B, H, N >= 1.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ * The bf16 path is one persistent kernel (one CTA per SM) whose CTAs draw
+ * Q-tile pairs from a work counter: the call enqueues a 4-byte
+ * cudaMemsetAsync of that counter on `stream`, then the kernel.  Counters
+ * are a fixed set of 64 per device, used round robin, so at most 64 bf16
+ * attn_fwd launches may be in flight at once across streams of one device
+ * (launches on one stream reuse counters in order and are always safe).
  */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int D, int causal, float scale, int dtype,
