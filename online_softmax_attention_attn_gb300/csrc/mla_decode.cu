@@ -69,6 +69,9 @@ constexpr int kRopeRowBytes = kRopeCols * 2;        // 64 B
 constexpr int kQropeBytes = kHq * kRopeRowBytes;    // q's RoPE half: 8 KB
 constexpr int kKropeBytes = kStep * kRopeRowBytes;  // a step's k_rope half: 4 KB
 constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
+static_assert((kStages & (kStages - 1)) == 0 && (kSBufs & (kSBufs - 1)) == 0 &&
+                  (kRopeSlots & (kRopeSlots - 1)) == 0,
+              "ring positions are taken with masks");
 constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
 // A received half is [token quad q][head][4 tokens] fp32: 16 B per head and
 // quad, so one exchange-warp store covers 512 contiguous bytes (32 heads) --
@@ -443,12 +446,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       // S partial for global step gg: A = this CTA's q columns (TMEM), B = K atoms.
       auto issue_s = [&](int gg) -> bool {
-        const int slot = gg % kStages;
-        if (!mbar_wait(bar_kv_full(slot), (gg / kStages) & 1, abort_flag, err, kSiteKvFull, gg))
+        const uint32_t u = (uint32_t)gg;
+        const uint32_t slot = u & (kStages - 1);
+        if (!mbar_wait(bar_kv_full(slot), (u / kStages) & 1u, abort_flag, err, kSiteKvFull, gg))
           return false;
         tc_fence_after();
         const uint64_t kd = kdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-        const uint32_t tS = tbase + kColS + (gg % kSBufs) * 64;
+        const uint32_t tS = tbase + kColS + (u & (kSBufs - 1)) * 64;
         // c_kv atoms: q from TMEM; the RoPE half: q from shared memory
         for (int a = 0; a < 4; ++a) {
 #pragma unroll
@@ -457,14 +461,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    kIdescS, (a | kk) != 0);
         }
         {
-          const uint64_t rd = kropedesc0 + (uint64_t)(((gg % kRopeSlots) * kKropeBytes) >> 4);
+          const uint64_t rd = kropedesc0 + (uint64_t)(((u & (kRopeSlots - 1)) * kKropeBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kRopeCols / 16; ++kk)
             mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
                    kIdescS, 1u);
         }
-        tc_commit(bar_s_full(gg % kSBufs));
-        tc_commit(bar_rope_empty(gg % kRopeSlots));  // the RoPE slot is free
+        tc_commit(bar_s_full(u & (kSBufs - 1)));
+        tc_commit(bar_rope_empty(u & (kRopeSlots - 1)));  // the RoPE slot is free
+        return true;
+      };
+      // O[:, own columns] += P V for global step gg (P in TMEM over its S)
+      auto issue_pv = [&](int gg, uint32_t acc_first) -> bool {
+        const uint32_t u = (uint32_t)gg;
+        const uint32_t sb = u & (kSBufs - 1);
+        const uint32_t slot = u & (kStages - 1);
+        if (!mbar_wait(bar_p_full(sb), (u / kSBufs) & 1u, abort_flag, err, kSitePFull, gg))
+          return false;
+        tc_fence_after();
+        const uint64_t vd = vdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
+        const uint32_t aP = tbase + kColS + sb * 64;
+        mma_ts(tO, aP, vd, kIdescPV, acc_first);
+#pragma unroll
+        for (int kk = 1; kk < kStep / 16; ++kk)
+          mma_ts(tO, aP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
+        tc_commit(bar_kv_empty(slot));
+        tc_commit(bar_pv_done);
         return true;
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
@@ -482,25 +504,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar_o_free, (seg_i - 1) & 1, abort_flag, err, kSitePvDone, seg_i);
             tc_fence_after();
           }
-          for (int i = 0; i < n && ok; ++i) {
-            const int gi = g + i;
-            ok = mbar_wait(bar_p_full(gi % kSBufs), (gi / kSBufs) & 1, abort_flag, err, kSitePFull, gi);
-            if (!ok) break;
-            tc_fence_after();
-            const int slot = gi % kStages;
-            const uint64_t vd = vdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kStep / 16; ++kk)
-              mma_ts(tO, tbase + kColS + (gi % kSBufs) * 64 + kk * 8,
-                     vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar_kv_empty(slot));
-            tc_commit(bar_pv_done);
-            if (i == n - 1) tc_commit(bar_o_ready);
-            if (i + kSBufs < n) {
-              ok = issue_s(gi + kSBufs);
+          // step 0 (O starts from zero), then steady steps whose S two ahead
+          // is never the segment's last, then a tail of at most three steps
+          // that carries the hand-over commits: no branches in the steady
+          // part, where every instruction of this thread delays the pipe
+          if (ok) ok = issue_pv(g, 0u);
+          if (ok && n > kSBufs) {
+            ok = issue_s(g + kSBufs);
+            if (ok && n == kSBufs + 1) tc_commit(bar_q_free);
+          }
+          int i = 1;
+          for (; i + kSBufs + 1 < n && ok; ++i) {
+            ok = issue_pv(g + i, 1u);
+            if (ok) ok = issue_s(g + i + kSBufs);
+          }
+          for (; i < n && ok; ++i) {
+            ok = issue_pv(g + i, 1u);
+            if (ok && i + kSBufs < n) {
+              ok = issue_s(g + i + kSBufs);
               if (ok && i + kSBufs == n - 1) tc_commit(bar_q_free);
             }
           }
+          if (ok) tc_commit(bar_o_ready);  // after the segment's last PV
           g += n;
           ++seg_i;
         }
