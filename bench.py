@@ -9,7 +9,8 @@ from CUDA events on the launching stream; an L2 flush (a 512 MiB write)
 separates timed steps.  `--workload` selects another single path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload step|prefill|decode|decode_paged|fp32|fp32_causal]
+                  [--workload step|prefill|prefill_noncausal|decode|decode_paged|
+                              decode_b16|decode_b128|decode_b256|fp32|fp32_causal]
 
 Multi-GPU: the path shards into independent problems, and every box here has
 one GPU, so N ranks run N independent replicas (weak scaling); value sums
@@ -284,6 +285,12 @@ def make_leg(name, dev):
         return DecodeLeg(I.MLA_B64, dev)
     if name == "decode_paged":
         return DecodeLeg(I.MLA_B256_PAGED, dev)
+    if name == "decode_b16":
+        return DecodeLeg(I.MLA_B16, dev)
+    if name == "decode_b128":
+        return DecodeLeg(I.MLA_B128, dev)
+    if name == "decode_b256":
+        return DecodeLeg(I.MLA_B256, dev)
     raise ValueError(name)
 
 
@@ -396,7 +403,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="step",
-                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged", "fp32",
+                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged", "decode_b16", "decode_b128", "decode_b256", "fp32",
                              "fp32_causal"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -56,7 +56,6 @@ constexpr int kPage = 64;
 constexpr int kStep = 64;                 // tokens per MMA step (one page)
 constexpr int kHalf = 32;                 // tokens per partial-S exchange
 constexpr int kThreads = 320;             // softmax, producer, MMA, exchange warps
-constexpr int kQAtomBytes = kHq * 128;    // 128 heads x 64 bf16
 constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
 constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
 constexpr int kStages = 4;
@@ -101,7 +100,7 @@ constexpr uint32_t kColS = 384;   // 2 x 64 columns
 
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
-  size_t header, prefix, bounds, plse, po, total;
+  size_t header, prefix, bounds, clist, plse, po, total;
   int max_chunks;
 };
 
@@ -113,7 +112,8 @@ __host__ __device__ constexpr WsLayout ws_layout(int B, int max_chunks) {
   w.header = 0;
   w.prefix = 64;
   w.bounds = align_up(w.prefix + sizeof(int) * (size_t)(B + 1), 16);
-  w.plse = align_up(w.bounds + sizeof(int) * (size_t)(max_chunks + 1), 256);
+  w.clist = align_up(w.bounds + sizeof(int) * (size_t)(max_chunks + 1), 16);
+  w.plse = align_up(w.clist + sizeof(int4) * (size_t)B, 256);
   w.po = align_up(w.plse + sizeof(float) * (size_t)(2 * max_chunks) * kHq, 256);
   w.total = align_up(w.po + sizeof(float) * (size_t)(2 * max_chunks) * kHq * kDv, 256);
   return w;
@@ -147,10 +147,12 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
                                                         int B, int max_blocks, int clusters,
                                                         int pps_override, int* __restrict__ hdr,
                                                         int* __restrict__ prefix,
-                                                        int* __restrict__ bounds, int* err) {
+                                                        int* __restrict__ bounds,
+                                                        int4* __restrict__ clist, int* err) {
   __shared__ int warp_sums[32];
   __shared__ int warp_max[32];
   __shared__ int carry, maxn_s, nchunks_s, pps_s, mode_s;
+  grid_launch_dependents();  // the decode kernel may set itself up meanwhile
   if (threadIdx.x == 0) { carry = 0; maxn_s = 0; }
   __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -245,6 +247,56 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     }
     bounds[k] = x;
   }
+  // The sequences the combine kernel has to finish, in order: empty ones
+  // (O = 0, LSE = -inf) and those cut by a chunk edge (partials to merge).
+  // Every other sequence is written whole by the decode kernel.
+  __syncthreads();  // every chunk edge is in place
+  __shared__ int ccarry;
+  if (threadIdx.x == 0) ccarry = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int f = 0, k0 = -1, k1 = -1;
+    if (b < B) {
+      const int pb = prefix[b], pe = prefix[b + 1];
+      if (pe == pb) {
+        f = 1;
+      } else {
+        k0 = find_range(bounds, nchunks, pb);
+        k1 = find_range(bounds, nchunks, pe - 1);
+        f = k0 != k1;
+      }
+    }
+    int x = f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + ccarry;
+    if (f) {
+      // {sequence, first chunk, last chunk, slot of the first chunk's partial}
+      // (a chunk's second segment writes slot 2k + 1); k0 = -1: empty sequence
+      const int first_slot = (k0 >= 0) ? (bounds[k0] != prefix[b] ? 2 * k0 + 1 : 2 * k0) : -1;
+      clist[incl - 1] = make_int4(b, k0, k1, first_slot);
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) ccarry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) hdr[4] = ccarry;
 }
 
 // ---- decode -----------------------------------------------------------------
@@ -305,8 +357,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
-  const int nchunks = hdr[1];
-  if (cluster >= nchunks) return;  // both CTAs of the cluster leave together
 
   // columns owned by this CTA: four 64-column c_kv atoms of the 576-wide row
   // and one half of the RoPE columns
@@ -375,6 +425,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers are initialised before any remote store
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // The set-up above overlaps the plan kernel; its chunk list is read only
+  // now.  A cluster without a chunk runs no role loop and goes to teardown.
+  grid_dependency_wait();
+  grid_launch_dependents();  // the combine kernel may be scheduled
+  const int nchunks = hdr[1];
 
   if (warp == 4) {
     // ================= producer: paged K/V (own columns) =================
@@ -646,11 +701,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         {
           const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + r) * kDk);
+          // all of this head's 256 columns in flight at once (one memory
+          // latency per segment, not one per atom), then into TMEM
+          uint4 qv[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) qv[c] = __ldg(qrow + atom_col(0) / 8 + c);
+#pragma unroll
           for (int a = 0; a < 4; ++a) {
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-              const uint4 v = __ldg(qrow + atom_col(a) / 8 + c);
+              const uint4 v = qv[a * 8 + c];
               w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
             }
             tmem_st32(tQ + a * 32, w);
@@ -881,62 +942,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---- combine ------------------------------------------------------------------
-// One CTA per (sequence, 16 heads).  Sequences inside one chunk were written
-// by the decode kernel; empty sequences get O = 0, LSE = -inf; the rest merge
-// their partials: L = log sum_s e^{L_s}, O = sum_s e^{L_s - L} O_s.
+// A fixed grid walks the (sequence, head) rows of the sequences the plan
+// listed, one warp per row and 16 output columns per lane: empty sequences
+// get O = 0, LSE = -inf; cut ones merge their partials,
+// L = log sum_s e^{L_s}, O = sum_s e^{L_s - L} O_s.  The plan has already
+// found each listed sequence's chunk range, so a row is a few independent
+// loads deep.  With nothing listed every block exits at once.
 __global__ void __launch_bounds__(256) mla_combine_kernel(
-    const int* __restrict__ hdr, const int* __restrict__ prefix, const int* __restrict__ bounds,
+    const int* __restrict__ hdr, const int* __restrict__ bounds, const int4* __restrict__ clist,
     const float* __restrict__ part_lse, const float* __restrict__ part_o,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
-  const int b = blockIdx.x;
-  const int h = blockIdx.y * 16 + (threadIdx.x >> 4);
-  const int c0 = (threadIdx.x & 15) * 32;
-  const int nchunks = hdr[1];
-  const int pb = prefix[b], pe = prefix[b + 1];
-  const size_t orow = (size_t)b * kHq + h;
-  if (pe == pb) {
-    for (int c = 0; c < 32; c += 8)
-      *reinterpret_cast<uint4*>(o + orow * kDv + c0 + c) = make_uint4(0u, 0u, 0u, 0u);
-    if (c0 == 0) lse[orow] = -INFINITY;
-    return;
-  }
-  const int k0 = find_range(bounds, nchunks, pb);
-  const int k1 = find_range(bounds, nchunks, pe - 1);
-  if (k0 == k1) return;  // written directly by the decode kernel
-  auto slot_of = [&](int k) { return (k == k0 && bounds[k0] != pb) ? 2 * k + 1 : 2 * k; };
-  float mx = -INFINITY;
-  for (int k = k0; k <= k1; ++k) {
-    if (bounds[k] == bounds[k + 1]) continue;
-    mx = fmaxf(mx, part_lse[(size_t)slot_of(k) * kHq + h]);
-  }
-  float acc[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-  float wsum = 0.f;
-  for (int k = k0; k <= k1; ++k) {
-    if (bounds[k] == bounds[k + 1]) continue;
-    const int slot = slot_of(k);
-    const float ls = part_lse[(size_t)slot * kHq + h];
-    const float w = (ls == -INFINITY) ? 0.f : expf(ls - mx);
-    wsum += w;
-    const float* src = part_o + ((size_t)slot * kHq + h) * kDv + c0;
-#pragma unroll
-    for (int c = 0; c < 32; c += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src + c);
-      acc[c] += w * v.x; acc[c + 1] += w * v.y; acc[c + 2] += w * v.z; acc[c + 3] += w * v.w;
+  grid_dependency_wait();  // the decode kernel's partials are complete
+  const int rows = hdr[4] * kHq;
+  const int lane = threadIdx.x & 31;
+  const int c0 = lane * 16;
+  for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8) {
+    const int4 e = clist[row / kHq];  // {b, k0, k1, first slot}
+    const int h = row % kHq;
+    const size_t orow = (size_t)e.x * kHq + h;
+    uint4* dst = reinterpret_cast<uint4*>(o + orow * kDv + c0);
+    if (e.y < 0) {
+      dst[0] = make_uint4(0u, 0u, 0u, 0u);
+      dst[1] = make_uint4(0u, 0u, 0u, 0u);
+      if (lane == 0) lse[orow] = -INFINITY;
+      continue;
     }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int k0 = e.y, k1 = e.z, s0 = e.w;
+    auto slot_of = [k0, s0](int k) { return k == k0 ? s0 : 2 * k; };
+    float mx = -INFINITY;
+    for (int k = k0; k <= k1; ++k) {
+      if (bounds[k] == bounds[k + 1]) continue;  // an empty chunk wrote nothing
+      mx = fmaxf(mx, part_lse[(size_t)slot_of(k) * kHq + h]);
+    }
+    float acc[16];
 #pragma unroll
-  for (int c = 0; c < 32; c += 8) {
-    uint4 wv;
-    wv.x = pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
-    wv.y = pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
-    wv.z = pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
-    wv.w = pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
-    *reinterpret_cast<uint4*>(o + orow * kDv + c0 + c) = wv;
+    for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    for (int k = k0; k <= k1; ++k) {
+      if (bounds[k] == bounds[k + 1]) continue;
+      const int slot = slot_of(k);
+      const float ls = part_lse[(size_t)slot * kHq + h];
+      const float w = (ls == -INFINITY) ? 0.f : expf(ls - mx);
+      wsum += w;
+      const float4* src =
+          reinterpret_cast<const float4*>(part_o + ((size_t)slot * kHq + h) * kDv + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        acc[4 * q] += w * v.x; acc[4 * q + 1] += w * v.y;
+        acc[4 * q + 2] += w * v.z; acc[4 * q + 3] += w * v.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      dst[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
+                          pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                          pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                          pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+    if (lane == 0) lse[orow] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
   }
-  if (c0 == 0) lse[orow] = (wsum > 0.f) ? mx + logf(wsum) : -INFINITY;
 }
 
 // The latent pool as a 2-D tensor [rows, 576]: boxes of `box_cols` columns x
@@ -1002,6 +1067,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   int* hdr = reinterpret_cast<int*>(ws + w.header);
   int* prefix = reinterpret_cast<int*>(ws + w.prefix);
   int* bounds = reinterpret_cast<int*>(ws + w.bounds);
+  int4* clist = reinterpret_cast<int4*>(ws + w.clist);
   float* plse = reinterpret_cast<float*>(ws + w.plse);
   float* po = reinterpret_cast<float*>(ws + w.po);
 
@@ -1014,18 +1080,36 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   mla_plan_kernel<<<1, 1024, 0, s>>>(a.seqlens, a.B, a.max_blocks, clusters, a.pages_per_split,
-                                     hdr, prefix, bounds, a.err);
+                                     hdr, prefix, bounds, clist, a.err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  mla_decode_kernel<<<2 * clusters, kThreads, kSmemBytes, s>>>(
-      mkv, mrope, static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
-      static_cast<__nv_bfloat16*>(a.o), a.lse, hdr, prefix, bounds, plse, po, a.B, a.max_blocks,
-      a.num_blocks, scale_log2, a.err);
-  e = cudaGetLastError();
+  // decode and combine are launched as programmatic dependents of the kernel
+  // before them: each starts while its predecessor finishes and waits for it
+  // (griddepcontrol.wait) only where it reads that kernel's output
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, mkv, mrope,
+                         static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
+                         static_cast<__nv_bfloat16*>(a.o), a.lse, (const int*)hdr,
+                         (const int*)prefix, (const int*)bounds, plse, po, a.B, a.max_blocks,
+                         a.num_blocks, scale_log2, a.err);
   if (e != cudaSuccess) return e;
-  mla_combine_kernel<<<dim3(a.B, kHq / 16), 256, 0, s>>>(hdr, prefix, bounds, plse, po,
-                                                         static_cast<__nv_bfloat16*>(a.o), a.lse);
+  cfg.gridDim = dim3(4 * a.num_sms, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, (const int*)hdr, (const int*)bounds,
+                         (const int4*)clist, (const float*)plse, (const float*)po,
+                         static_cast<__nv_bfloat16*>(a.o), a.lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -48,6 +48,21 @@ __device__ __forceinline__ bool named_barrier_any(uint32_t id, uint32_t nthreads
   return r != 0;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Block until every grid this one depends on (through a launch with
+// programmatic stream serialisation) has completed and its writes are
+// visible.  A no-op for a grid launched without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the grid that depends on this one be scheduled now (its CTAs still
+// wait for this grid's completion before reading what it wrote).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -72,6 +72,10 @@ MLA_B64 = MLAConfig("bf16 MLA decode batch64 Hq128 seq4096", 64, 128, 4096,
                     4096, False, 1004)
 MLA_B256_PAGED = MLAConfig("bf16 MLA decode batch256 Hq128 seq1024-4096 paged",
                            256, 128, 1024, 4096, True, 1005)
+# The decode batch sweep at seq 4096 (batch 64 is MLA_B64 above).
+MLA_B16 = MLAConfig("bf16 MLA decode batch16 Hq128 seq4096", 16, 128, 4096, 4096, False, 1006)
+MLA_B128 = MLAConfig("bf16 MLA decode batch128 Hq128 seq4096", 128, 128, 4096, 4096, False, 1007)
+MLA_B256 = MLAConfig("bf16 MLA decode batch256 Hq128 seq4096", 256, 128, 4096, 4096, False, 1008)
 
 
 def _gen(seed: int) -> torch.Generator:

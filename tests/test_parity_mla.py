@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import online_softmax_attention_attn_gb300 as pkg
-from online_softmax_attention_attn_gb300.inputs import (MLA_B64, MLA_B256_PAGED,
+from online_softmax_attention_attn_gb300.inputs import (MLA_B16, MLA_B64, MLA_B128, MLA_B256,
+                                                         MLA_B256_PAGED,
                                                          mla_config_inputs, mla_inputs)
 
 pytestmark = pytest.mark.gpu
@@ -170,3 +171,10 @@ def test_decode_batch64_workload_sampled():
 
 def test_decode_batch256_paged_workload_sampled():
     _sampled(MLA_B256_PAGED, 192, 2)
+
+
+@pytest.mark.parametrize("cfg", [MLA_B16, MLA_B128, MLA_B256], ids=lambda c: str(c.batch))
+def test_decode_batch_sweep_sampled(cfg):
+    """The batch sweep at seq 4096: batch 16 runs through the split-KV plan
+    (fewer sequences than clusters), 128 and 256 through whole chunks."""
+    _sampled(cfg, 128, 3)
