@@ -10,7 +10,7 @@ separates timed steps.  `--workload` selects another single path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload step|prefill|prefill_noncausal|decode|decode_paged|
-                              decode_b16|decode_b128|decode_b256|fp32|fp32_causal]
+                              decode_b16|decode_b128|decode_b256|mla_layer|fp32|fp32_causal]
 
 Multi-GPU: the path shards into independent problems, and every box here has
 one GPU, so N ranks run N independent replicas (weak scaling); value sums
@@ -272,6 +272,68 @@ class DecodeLeg:
         return sample_bytes / dt / 1e9, desc, dt
 
 
+class LayerLeg(DecodeLeg):
+    """One MLA attention layer: the absorbed query (q_nope W_UK | q_rope), the
+    latent decode, and each head's value projection O_latent W_UV.  Weights
+    stay resident; the bytes count the cache, both weight sets and every
+    activation read or written once."""
+
+    def __init__(self, cfg: I.MLAConfig, dev):
+        super().__init__(cfg, dev)
+        B, Hq = cfg.batch, cfg.Hq
+        (self.qn, self.qr, self.wk, self.wv, _, _, _) = I.mla_layer_inputs(
+            B, Hq, self.sl, seed=cfg.seed)
+        self.dqn, self.dqr, self.dwk, self.dwv = (t.to(dev) for t in
+                                                  (self.qn, self.qr, self.wk, self.wv))
+        self.qa = torch.empty(B, Hq, 576, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(B, Hq, I.MLA_DVHEAD, dtype=torch.bfloat16, device=dev)
+        e = 2
+        proj = (self.wk.numel() + self.wv.numel() + self.qn.numel() + self.qr.numel()
+                + self.qa.numel() + self.o.numel() + self.out.numel()) * e
+        self.bytes = self.bytes + proj
+        self.flops = self.flops + 2.0 * B * Hq * (I.MLA_DNOPE * 512 + 512 * I.MLA_DVHEAD)
+
+    def run(self):
+        self.pkg.mla_absorb_q(self.dqn, self.dqr, self.dwk, q_out=self.qa)
+        self.pkg.mla_decode(self.qa, self.dkv, self.dtable, self.dsl, self.o, self.lse,
+                            scale=self.cfg.scale, workspace=self.ws)
+        self.pkg.mla_project_out(self.o, self.dwv, out=self.out)
+
+    def e2e_setup(self):
+        super().e2e_setup()
+        self.hqn, self.hqr = (t.pin_memory() for t in (self.qn, self.qr))
+        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = (self.h2d - self.hq.numel() * 2 + self.hqn.numel() * 2 + self.hqr.numel() * 2)
+        self.d2h = self.hout.numel() * 2 + self.hl.numel() * 4
+
+    def e2e_run(self):
+        self.dqn.copy_(self.hqn, non_blocking=True)
+        self.dqr.copy_(self.hqr, non_blocking=True)
+        self.dkv.copy_(self.hkv, non_blocking=True)
+        self.dtable.copy_(self.htable, non_blocking=True)
+        self.dsl.copy_(self.hsl, non_blocking=True)
+        self.run()
+        self.hout.copy_(self.out, non_blocking=True)
+        self.hl.copy_(self.lse, non_blocking=True)
+
+    def workload_name(self):
+        return "bf16 MLA layer (absorb + decode + project) batch64 Hq128 seq4096"
+
+    def oracle_sample(self, budget_s: float, threads: int):
+        import oracle
+        c = self.cfg
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle.mla_decompressed(self.qn[n:n + 1], self.qr[n:n + 1], self.wk, self.wv,
+                                    self.kv, self.table[n:n + 1], self.sl[n:n + 1], c.scale)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s or n >= c.batch:
+                break
+        desc = f"{n} of {c.batch} sequences, all {c.Hq} heads, keys and values decompressed"
+        return self.bytes * (n / c.batch) / dt / 1e9, desc, dt
+
+
 def make_leg(name, dev):
     if name == "prefill":
         return PrefillLeg(I.BF16_PREFILL, dev)
@@ -285,6 +347,8 @@ def make_leg(name, dev):
         return DecodeLeg(I.MLA_B64, dev)
     if name == "decode_paged":
         return DecodeLeg(I.MLA_B256_PAGED, dev)
+    if name == "mla_layer":
+        return LayerLeg(I.MLA_B64, dev)
     if name == "decode_b16":
         return DecodeLeg(I.MLA_B16, dev)
     if name == "decode_b128":
@@ -387,7 +451,7 @@ def config_of(workload, leg):
                "dtype": "bf16" if c.dtype == torch.bfloat16 else "fp32"}
     else:
         c = leg.cfg
-        cfg = {"workload": c.name, "batch": c.batch, "Hq": c.Hq, "seq_min": c.seq_min,
+        cfg = {"workload": leg.workload_name(), "batch": c.batch, "Hq": c.Hq, "seq_min": c.seq_min,
                "seq_max": c.seq_max, "page": 64, "paged_random": c.paged_random}
     if workload == "step":
         cfg["workload"] = ("step = " + I.BF16_PREFILL.name + " + " + I.MLA_B64.name)
@@ -403,7 +467,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="step",
-                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged", "decode_b16", "decode_b128", "decode_b256", "fp32",
+                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged",
+                             "decode_b16", "decode_b128", "decode_b256", "mla_layer", "fp32",
                              "fp32_causal"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

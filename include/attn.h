@@ -185,6 +185,42 @@ ATTN_API int mla_decode_noalloc(const void* q, const void* kv_cache,
                                 void* stream);
 
 /*
+ * mla_absorb_q -- the absorbed query that mla_decode takes ("MLA x
+ * FlashAttention-3 fusion" article: the absorption identity
+ * Q K^T = (Q W_UK) c^T + Q_R k_R^T, which folds W_UK into the query).
+ *
+ *   q_nope   : [B, Hq, d_nope] bf16, the non-rotary part of each head's query.
+ *   q_rope   : [B, Hq, d_rope] bf16, the rotary part (passed through).
+ *   w_uk     : [Hq, d_nope, d_latent] bf16, each head's key up-projection
+ *              (key_nope_h = c W_UK_h^T for a latent row c).
+ *   q_out    : [B, Hq, d_latent + d_rope] bf16 (written):
+ *              [q_nope_h W_UK_h | q_rope_h]; mla_decode takes d_latent = 512,
+ *              d_rope = 64.
+ * One strided-batched cuBLAS GEMM over the Hq heads (fp32 accumulation,
+ * bf16 result) and a strided copy, both on `stream`.  The first call on a
+ * device creates that device's cuBLAS handle (which allocates its workspace
+ * once); calls from several host threads are serialised internally.
+ * Requirements: pointers non-null and 16-byte aligned; every width a
+ * multiple of 8.  Errors: INVALID_ARG, MISALIGNED, CUDA.
+ */
+ATTN_API int mla_absorb_q(const void* q_nope, const void* q_rope, const void* w_uk,
+                          void* q_out, int B, int Hq, int d_nope, int d_rope, int d_latent,
+                          void* stream);
+
+/*
+ * mla_project_out -- each head's output from mla_decode's latent output:
+ * out_h = o_latent_h W_UV_h (the value up-projection the article's fused
+ * kernel applies after the latent attention).
+ *
+ *   o_latent : [B, Hq, d_latent] bf16 (mla_decode's o; d_latent = 512).
+ *   w_uv     : [Hq, d_latent, d_v] bf16, each head's value up-projection.
+ *   out      : [B, Hq, d_v] bf16 (written).
+ * Same execution, requirements and errors as mla_absorb_q.
+ */
+ATTN_API int mla_project_out(const void* o_latent, const void* w_uv, void* out, int B, int Hq,
+                             int d_latent, int d_v, void* stream);
+
+/*
  * attn_device_status -- synchronise `stream`, then return and clear the
  * device error word of the current device (ATTN_OK if no kernel recorded an
  * error since the last call).  attn_last_error() then names the failing check.

@@ -22,7 +22,8 @@ import os
 
 __all__ = [
     "AttnError", "lib", "attn_fwd", "mla_decode", "mla_decode_split",
-    "mla_decode_workspace_size", "mla_decode_noalloc", "attn_device_status", "attn_last_error",
+    "mla_decode_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
+    "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
     "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
 ]
@@ -79,6 +80,10 @@ def lib():
         L.mla_decode_split.restype = _i
         L.mla_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp]
         L.mla_decode_noalloc.restype = _i
+        L.mla_absorb_q.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+        L.mla_absorb_q.restype = _i
+        L.mla_project_out.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        L.mla_project_out.restype = _i
         L.attn_device_status.argtypes = [_vp]
         L.attn_device_status.restype = _i
         L.attn_last_error.argtypes = []
@@ -236,6 +241,43 @@ def mla_decode_noalloc(q, kv_cache, block_table, seqlens, o=None, lse=None,
                                     _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, float(scale),
                                     block_table.shape[1], nb, _stream_ptr(stream)))
     return o, lse
+
+
+def mla_absorb_q(q_nope, q_rope, w_uk, q_out=None, stream=None):
+    """The absorbed query [q_nope_h W_UK_h | q_rope_h] that mla_decode takes.
+
+    q_nope [B,Hq,d_nope], q_rope [B,Hq,d_rope], w_uk [Hq,d_nope,d_latent], bf16.
+    Returns q_out [B,Hq,d_latent+d_rope] bf16.
+    """
+    import torch
+    B, Hq, d_nope = q_nope.shape
+    d_rope = q_rope.shape[2]
+    d_latent = w_uk.shape[2]
+    _require(q_nope, "q_nope", torch.bfloat16, (B, Hq, d_nope))
+    _require(q_rope, "q_rope", torch.bfloat16, (B, Hq, d_rope))
+    _require(w_uk, "w_uk", torch.bfloat16, (Hq, d_nope, d_latent))
+    if q_out is None:
+        q_out = torch.empty(B, Hq, d_latent + d_rope, dtype=torch.bfloat16, device=q_nope.device)
+    _require(q_out, "q_out", torch.bfloat16, (B, Hq, d_latent + d_rope))
+    _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(q_out), B, Hq,
+                              d_nope, d_rope, d_latent, _stream_ptr(stream)))
+    return q_out
+
+
+def mla_project_out(o_latent, w_uv, out=None, stream=None):
+    """Each head's output o_latent_h W_UV_h.  o_latent [B,Hq,d_latent], w_uv
+    [Hq,d_latent,d_v], bf16; returns out [B,Hq,d_v] bf16."""
+    import torch
+    B, Hq, d_latent = o_latent.shape
+    d_v = w_uv.shape[2]
+    _require(o_latent, "o_latent", torch.bfloat16, (B, Hq, d_latent))
+    _require(w_uv, "w_uv", torch.bfloat16, (Hq, d_latent, d_v))
+    if out is None:
+        out = torch.empty(B, Hq, d_v, dtype=torch.bfloat16, device=o_latent.device)
+    _require(out, "out", torch.bfloat16, (B, Hq, d_v))
+    _check(lib().mla_project_out(_ptr(o_latent), _ptr(w_uv), _ptr(out), B, Hq, d_latent, d_v,
+                                 _stream_ptr(stream)))
+    return out
 
 
 def attn_device_status(stream=None, raise_on_error: bool = True) -> int:

@@ -1,8 +1,9 @@
 """Build step for libattn.so: nvcc, sm_103a only, in-tree.
 
 Each .cu file under csrc/ is compiled to an object in parallel, then linked
-into ``libattn.so`` next to this file.  The CUDA runtime is linked statically,
-so the library needs only the driver at run time.
+into ``libattn.so`` next to this file.  The CUDA runtime is linked statically;
+cuBLAS (used for the absorption GEMMs only) is linked from the toolkit with
+its directory recorded as the run-time search path.
 """
 from __future__ import annotations
 
@@ -17,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_api.cu", "prefill_f32.cu", "prefill_bf16.cu", "mla_decode.cu"]
+SOURCES = ["attn_api.cu", "prefill_f32.cu", "prefill_bf16.cu", "mla_decode.cu",
+           "mla_absorb.cu"]
 
 
 def nvcc_path() -> str:
@@ -56,7 +58,11 @@ def build(verbose_ptxas: bool = False, quiet: bool = True) -> str:
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + ".tmp"
-    cmd = [nvcc_path(), *ARCH, "-shared", *objs, "-o", tmp]
+    # cuBLAS (the absorption GEMMs) from the toolkit next to nvcc, found at
+    # run time through the recorded path
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc_path())), "lib64")
+    cmd = [nvcc_path(), *ARCH, "-shared", *objs, "-o", tmp, "-L", cuda_lib, "-lcublas",
+           "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

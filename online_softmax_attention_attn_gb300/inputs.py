@@ -102,7 +102,7 @@ def mha_config_inputs(cfg: MHAConfig):
 def mla_inputs(batch: int, Hq: int, seqlens, seed: int = 0,
                paged_random: bool = False, q_std: float = 1.0,
                cache_std: float = 0.5, num_blocks: int | None = None,
-               max_blocks: int | None = None, dtype=torch.bfloat16):
+               max_blocks: int | None = None, dtype=torch.bfloat16, width: int = MLA_DK):
     """Absorbed queries, a paged latent pool, a block table and lengths (CPU).
 
     q [batch, Hq, 576]; kv_cache [num_blocks, 64, 576] filled over the whole
@@ -115,8 +115,8 @@ def mla_inputs(batch: int, Hq: int, seqlens, seed: int = 0,
     need = int(math.ceil(int(seqlens.max().item() if batch else 0) / MLA_PAGE))
     max_blocks = max(need, 1) if max_blocks is None else max_blocks
     num_blocks = batch * max_blocks if num_blocks is None else num_blocks
-    q = torch.randn(batch, Hq, MLA_DK, generator=g, dtype=torch.float32) * q_std
-    kv = torch.randn(num_blocks, MLA_PAGE, MLA_DK, generator=g,
+    q = torch.randn(batch, Hq, width, generator=g, dtype=torch.float32) * q_std
+    kv = torch.randn(num_blocks, MLA_PAGE, width, generator=g,
                      dtype=torch.float32) * cache_std
     if paged_random:
         perm = torch.randperm(num_blocks, generator=g)[: batch * max_blocks]
@@ -126,6 +126,33 @@ def mla_inputs(batch: int, Hq: int, seqlens, seed: int = 0,
             batch, max_blocks)
     return (q.to(dtype).contiguous(), kv.to(dtype).contiguous(),
             table.contiguous(), seqlens.contiguous())
+
+
+# Widths of the projections around the latent attention (DeepSeek-style MLA):
+# per head a 128-wide non-rotary query part, a 64-wide rotary part, a
+# 512-wide latent and a 128-wide value.
+MLA_DNOPE, MLA_DROPE, MLA_DLATENT, MLA_DVHEAD = 128, 64, 512, 128
+
+
+def mla_layer_inputs(batch: int, Hq: int, seqlens, seed: int = 0, d_nope: int = MLA_DNOPE,
+                     d_rope: int = MLA_DROPE, d_latent: int = MLA_DLATENT,
+                     d_v: int = MLA_DVHEAD, paged_random: bool = False,
+                     cache_std: float = 0.5, dtype=torch.bfloat16):
+    """Un-absorbed query parts, per-head up-projections and a paged latent pool (CPU).
+
+    q_nope [batch,Hq,d_nope], q_rope [batch,Hq,d_rope] ~ N(0,1);
+    w_uk [Hq,d_nope,d_latent] ~ N(0,1/d_nope), w_uv [Hq,d_latent,d_v] ~ N(0,1/d_latent)
+    (so projected entries stay of order one); the cache, block table and lengths
+    are those of ``mla_inputs`` (rows of d_latent + d_rope).
+    """
+    g = _gen(seed + 104729)
+    q_nope = torch.randn(batch, Hq, d_nope, generator=g, dtype=torch.float32)
+    q_rope = torch.randn(batch, Hq, d_rope, generator=g, dtype=torch.float32)
+    w_uk = torch.randn(Hq, d_nope, d_latent, generator=g, dtype=torch.float32) / math.sqrt(d_nope)
+    w_uv = torch.randn(Hq, d_latent, d_v, generator=g, dtype=torch.float32) / math.sqrt(d_latent)
+    _, kv, table, sl = mla_inputs(batch, Hq, seqlens, seed=seed, paged_random=paged_random,
+                                  cache_std=cache_std, dtype=dtype, width=d_latent + d_rope)
+    return (q_nope.to(dtype), q_rope.to(dtype), w_uk.to(dtype), w_uv.to(dtype), kv, table, sl)
 
 
 def mla_seqlens(cfg: MLAConfig) -> torch.Tensor:

@@ -167,3 +167,80 @@ def mla(q, kv_cache, block_table, seqlens, scale: float, dv: int = 512,
     if rows is None:
         return o.reshape(B, Hq, dv), lse.reshape(B, Hq)
     return o, lse
+
+
+# ----------------------------------------------------------------------------
+# The projections around the latent attention ("MLA x FlashAttention-3
+# fusion" article: absorption identity Q K^T = (Q W_UK) c^T + Q_R k_R^T, and
+# the value up-projection W_UV after the latent attention).  Plain fp64
+# definitions; numpy's matrix product is the library step.
+
+def _f64(x) -> np.ndarray:
+    """Exact widening to a contiguous float64 numpy array."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu").to(torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def mla_absorb_q(q_nope, q_rope, w_uk) -> np.ndarray:
+    """[q_nope_h W_UK_h | q_rope_h] for every sequence and head, fp64.
+
+    q_nope [B,Hq,Dn], q_rope [B,Hq,Dr], w_uk [Hq,Dn,L] -> [B,Hq,L+Dr].
+    """
+    qn, qr, w = _f64(q_nope), _f64(q_rope), _f64(w_uk)
+    B, Hq, _ = qn.shape
+    L = w.shape[2]
+    out = np.empty((B, Hq, L + qr.shape[2]), dtype=np.float64)
+    for h in range(Hq):
+        out[:, h, :L] = qn[:, h, :] @ w[h]
+    out[:, :, L:] = qr
+    return out
+
+
+def mla_project_out(o_latent, w_uv) -> np.ndarray:
+    """o_latent_h W_UV_h for every sequence and head, fp64: [B,Hq,L] x [Hq,L,Dv]."""
+    ol, w = _f64(o_latent), _f64(w_uv)
+    out = np.empty((ol.shape[0], ol.shape[1], w.shape[2]), dtype=np.float64)
+    for h in range(ol.shape[1]):
+        out[:, h, :] = ol[:, h, :] @ w[h]
+    return out
+
+
+def mla_decompressed(q_nope, q_rope, w_uk, w_uv, kv_cache, block_table, seqlens,
+                     scale: float):
+    """MLA attention with every head's keys and values decompressed, fp64.
+
+    Per sequence b and head h, over the visible tokens t of its pages:
+    K_h[t] = [c_t W_UK_h^T | k_rope_t], V_h[t] = c_t W_UV_h, and
+    out = softmax(scale * [q_nope_h | q_rope_h] K_h^T) V_h, with its natural-log
+    LSE.  This is attention as first defined, before any absorption; the
+    absorbed path (mla_absorb_q, mla, mla_project_out) must reproduce it.
+    Returns (out [B,Hq,Dv], lse [B,Hq]).
+    """
+    qn, qr, wk, wv = _f64(q_nope), _f64(q_rope), _f64(w_uk), _f64(w_uv)
+    cache = _f64(kv_cache)
+    bt, sl = _i32(block_table), _i32(seqlens)
+    B, Hq, _ = qn.shape
+    L = wk.shape[2]
+    page = cache.shape[1]
+    out = np.zeros((B, Hq, wv.shape[2]), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        n = int(sl[b])
+        if n == 0:
+            continue
+        rows = np.concatenate([cache[bt[b, j]] for j in range((n + page - 1) // page)])[:n]
+        c, kr = rows[:, :L], rows[:, L:]
+        for h in range(Hq):
+            k_h = np.concatenate([c @ wk[h].T, kr], axis=1)
+            v_h = c @ wv[h]
+            s = scale * (k_h @ np.concatenate([qn[b, h], qr[b, h]]))
+            m = s.max()
+            p = np.exp(s - m)
+            out[b, h] = (p @ v_h) / p.sum()
+            lse[b, h] = m + np.log(p.sum())
+    return out, lse

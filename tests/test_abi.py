@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
               "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
-              "attn_fwd_test_skip_load"]:
+              "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out"]:
         assert n in names
 
 
@@ -99,3 +99,20 @@ def test_kernel_info(L):
     assert bf["Br"] == 128 and bf["Bc"] == 128 and bf["smem_bytes"] <= 232448
     with pytest.raises(pkg.AttnError):
         pkg.attn_kernel_info(pkg.ATTN_DTYPE_F32, 80)
+
+
+def test_projection_arguments_are_checked_before_any_cuda_call(L):
+    """The absorption GEMMs reject bad arguments on the host (no GPU needed)."""
+    rc = L.mla_absorb_q(None, None, None, None, 4, 128, 128, 64, 512, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG and "null pointer" in pkg.attn_last_error()
+    import ctypes
+    buf = ctypes.create_string_buffer(256)
+    p = ctypes.cast(ctypes.addressof(buf), ctypes.c_void_p)
+    aligned = ctypes.c_void_p((p.value + 15) & ~15)
+    rc = L.mla_absorb_q(aligned, aligned, aligned, aligned, 4, 128, 100, 64, 512, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG and "multiples of 8" in pkg.attn_last_error()
+    rc = L.mla_project_out(aligned, aligned, aligned, 0, 128, 512, 128, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(aligned.value + 2)
+    rc = L.mla_project_out(odd, aligned, aligned, 4, 128, 512, 128, None)
+    assert rc == pkg.ATTN_ERR_MISALIGNED

@@ -416,3 +416,61 @@ def test_mutants_are_caught(oracle_lib, tmp_path):
         assert not _pins_pass(lib), f"pins missed the planted mistake: {name}"
         checked += 1
     assert checked >= 8
+
+
+# ---------------------------------------------------------------- MLA projections
+
+def _layer(seed=3, B=2, Hq=4, lens=(37, 70), dn=16, dr=8, dl=32, dv=16):
+    from online_softmax_attention_attn_gb300.inputs import mla_layer_inputs
+    return mla_layer_inputs(B, Hq, list(lens), seed=seed, d_nope=dn, d_rope=dr, d_latent=dl,
+                            d_v=dv, paged_random=True)
+
+
+def test_absorption_identity_matches_decompressed_attention(oracle_lib):
+    """The article's absorption identity: folding W_UK into the query and W_UV
+    after the latent attention gives exactly the attention over explicitly
+    decompressed keys [c W_UK^T | k_rope] and values c W_UV (fp64; the only
+    residue is the fp32 rounding of the absorbed query fed to the C oracle)."""
+    qn, qr, wk, wv, kv, table, sl = _layer()
+    qa = oracle.mla_absorb_q(qn, qr, wk)
+    ol, lse = oracle.mla(qa, kv, table, sl, 0.2, dv=32, lib=oracle_lib)
+    out = oracle.mla_project_out(ol, wv)
+    ref, rlse = oracle.mla_decompressed(qn, qr, wk, wv, kv, table, sl, 0.2)
+    assert np.abs(out - ref).max() <= 1e-6 * np.abs(ref).max()
+    assert np.abs(lse - rlse).max() <= 1e-6
+    # a planted slip: the rotary part left out of the absorbed query
+    qa_bad = qa.copy()
+    qa_bad[:, :, 32:] = 0.0
+    ol_bad, _ = oracle.mla(qa_bad, kv, table, sl, 0.2, dv=32, lib=oracle_lib)
+    assert np.abs(oracle.mla_project_out(ol_bad, wv) - ref).max() > 1e-3
+
+
+def test_absorb_and_project_with_identity_weights():
+    """W_UK = [I | 0] copies q_nope into the leading latent columns (rest zero,
+    q_rope appended); W_UV = [I; 0] keeps the leading latent columns."""
+    qn, qr, _, _, _, _, _ = _layer()
+    wk = np.zeros((4, 16, 32))
+    wk[:, :, :16] = np.eye(16)
+    qa = oracle.mla_absorb_q(qn, qr, wk)
+    assert np.array_equal(qa[:, :, :16], qn.float().numpy())
+    assert not qa[:, :, 16:32].any()
+    assert np.array_equal(qa[:, :, 32:], qr.float().numpy())
+    ol = np.random.default_rng(1).standard_normal((2, 4, 32))
+    wv = np.zeros((4, 32, 16))
+    wv[:, :16, :] = np.eye(16)
+    assert np.array_equal(oracle.mla_project_out(ol, wv), ol[:, :, :16])
+
+
+def test_decompressed_single_token_gives_its_value_row():
+    """One visible token: the attention output is that token's value row
+    c_0 W_UV_h and the LSE is the scaled score itself."""
+    qn, qr, wk, wv, kv, table, _ = _layer(lens=(1, 1))
+    sl = torch.tensor([1, 1], dtype=torch.int32)
+    out, lse = oracle.mla_decompressed(qn, qr, wk, wv, kv, table, sl, 0.3)
+    for b in range(2):
+        row = kv[int(table[b, 0]), 0].double().numpy()
+        for h in range(4):
+            assert np.allclose(out[b, h], row[:32] @ wv[h].double().numpy(), rtol=1e-12)
+            k = np.concatenate([row[:32] @ wk[h].double().numpy().T, row[32:]])
+            q = np.concatenate([qn[b, h].double().numpy(), qr[b, h].double().numpy()])
+            assert abs(lse[b, h] - 0.3 * float(k @ q)) <= 1e-9
