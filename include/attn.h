@@ -196,12 +196,14 @@ ATTN_API int mla_decode_noalloc(const void* q, const void* kv_cache,
  *   q_out    : [B, Hq, d_latent + d_rope] bf16 (written):
  *              [q_nope_h W_UK_h | q_rope_h]; mla_decode takes d_latent = 512,
  *              d_rope = 64.
- * One strided-batched cuBLAS GEMM over the Hq heads (fp32 accumulation,
- * bf16 result) and a strided copy, both on `stream`.  The first call on a
- * device creates that device's cuBLAS handle (which allocates its workspace
- * once); calls from several host threads are serialised internally.
+ * One kernel on `stream`: per (head, 128 output columns, 64 tokens) a
+ * tcgen05 product with fp32 accumulation and a bf16 result, plus the copy of
+ * q_rope.  It is launched as a programmatic dependent of the previous kernel
+ * on the stream and reads nothing before that kernel has completed.
  * Requirements: pointers non-null and 16-byte aligned; every width a
- * multiple of 8.  Errors: INVALID_ARG, MISALIGNED, CUDA.
+ * multiple of 8.  Built for d_nope a multiple of 64 up to 512 and d_latent a
+ * multiple of 64 (else UNSUPPORTED).  Errors: INVALID_ARG, UNSUPPORTED,
+ * MISALIGNED, CUDA.
  */
 ATTN_API int mla_absorb_q(const void* q_nope, const void* q_rope, const void* w_uk,
                           void* q_out, int B, int Hq, int d_nope, int d_rope, int d_latent,
@@ -215,7 +217,8 @@ ATTN_API int mla_absorb_q(const void* q_nope, const void* q_rope, const void* w_
  *   o_latent : [B, Hq, d_latent] bf16 (mla_decode's o; d_latent = 512).
  *   w_uv     : [Hq, d_latent, d_v] bf16, each head's value up-projection.
  *   out      : [B, Hq, d_v] bf16 (written).
- * Same execution, requirements and errors as mla_absorb_q.
+ * Same execution and errors as mla_absorb_q; built for d_latent a multiple of
+ * 64 up to 512 and d_v a multiple of 64.
  */
 ATTN_API int mla_project_out(const void* o_latent, const void* w_uv, void* out, int B, int Hq,
                              int d_latent, int d_v, void* stream);

@@ -1,9 +1,8 @@
 """Build step for libattn.so: nvcc, sm_103a only, in-tree.
 
 Each .cu file under csrc/ is compiled to an object in parallel, then linked
-into ``libattn.so`` next to this file.  The CUDA runtime is linked statically;
-cuBLAS (used for the absorption GEMMs only) is linked from the toolkit with
-its directory recorded as the run-time search path.
+into ``libattn.so`` next to this file.  The CUDA runtime is linked statically,
+so the library needs only the driver at run time.
 """
 from __future__ import annotations
 
@@ -58,11 +57,7 @@ def build(verbose_ptxas: bool = False, quiet: bool = True) -> str:
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + ".tmp"
-    # cuBLAS (the absorption GEMMs) from the toolkit next to nvcc, found at
-    # run time through the recorded path
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc_path())), "lib64")
-    cmd = [nvcc_path(), *ARCH, "-shared", *objs, "-o", tmp, "-L", cuda_lib, "-lcublas",
-           "-Xlinker", "-rpath=" + cuda_lib]
+    cmd = [nvcc_path(), *ARCH, "-shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -61,6 +61,8 @@ static int* device_err_word(int* code_out) {
   return g_err_ptr[dev];
 }
 
+int* attn_device_err_word(int* code_out) { return device_err_word(code_out); }
+
 static int sm_count(int* code_out) {
   int dev = 0, n = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -132,6 +132,9 @@ int mla_noalloc_max_sms();
 
 // Error-message helper shared by the host files.
 void attn_set_error(const char* fmt, ...);
+// The current device's error word (kernels record device-side failures in
+// it); nullptr with *code_out set when it cannot be found.
+int* attn_device_err_word(int* code_out);
 
 // Driver entry point for cuTensorMapEncodeTiled (resolved once through cudart).
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -152,7 +152,11 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   __shared__ int warp_sums[32];
   __shared__ int warp_max[32];
   __shared__ int carry, maxn_s, nchunks_s, pps_s, mode_s;
-  grid_launch_dependents();  // the decode kernel may set itself up meanwhile
+  // launched as a programmatic dependent of whatever precedes it on the
+  // stream: wait for it before reading the lengths, then let the decode
+  // kernel set itself up while this plan runs
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (threadIdx.x == 0) { carry = 0; maxn_s = 0; }
   __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -1079,10 +1083,20 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
     attn_set_error("mla_decode: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return cudaErrorInvalidValue;
   }
-  mla_plan_kernel<<<1, 1024, 0, s>>>(a.seqlens, a.B, a.max_blocks, clusters, a.pages_per_split,
-                                     hdr, prefix, bounds, clist, a.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  {
+    cudaLaunchAttribute pdl1[1];
+    pdl1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl1[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(1, 1, 1);
+    pc.blockDim = dim3(1024, 1, 1);
+    pc.stream = s;
+    pc.attrs = pdl1;
+    pc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pc, mla_plan_kernel, (const int32_t*)a.seqlens, a.B, a.max_blocks,
+                           clusters, a.pages_per_split, hdr, prefix, bounds, clist, a.err);
+    if (e != cudaSuccess) return e;
+  }
   const float scale_log2 = a.scale * 1.4426950408889634f;
   // decode and combine are launched as programmatic dependents of the kernel
   // before them: each starts while its predecessor finishes and waits for it
