@@ -100,7 +100,7 @@ constexpr uint32_t kColS = 384;   // 2 x 64 columns
 
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
-  size_t header, prefix, bounds, clist, plse, po, total;
+  size_t header, prefix, bounds, cstart, clist, plse, po, total;
   int max_chunks;
 };
 
@@ -112,7 +112,8 @@ __host__ __device__ constexpr WsLayout ws_layout(int B, int max_chunks) {
   w.header = 0;
   w.prefix = 64;
   w.bounds = align_up(w.prefix + sizeof(int) * (size_t)(B + 1), 16);
-  w.clist = align_up(w.bounds + sizeof(int) * (size_t)(max_chunks + 1), 16);
+  w.cstart = align_up(w.bounds + sizeof(int) * (size_t)(max_chunks + 1), 16);
+  w.clist = align_up(w.cstart + sizeof(int) * (size_t)max_chunks, 16);
   w.plse = align_up(w.clist + sizeof(int4) * (size_t)B, 256);
   w.po = align_up(w.plse + sizeof(float) * (size_t)(2 * max_chunks) * kHq, 256);
   w.total = align_up(w.po + sizeof(float) * (size_t)(2 * max_chunks) * kHq * kDv, 256);
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
                                                         int pps_override, int* __restrict__ hdr,
                                                         int* __restrict__ prefix,
                                                         int* __restrict__ bounds,
+                                                        int* __restrict__ cstart,
                                                         int4* __restrict__ clist, int* err) {
   __shared__ int warp_sums[32];
   __shared__ int warp_max[32];
@@ -250,6 +252,9 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
       }
     }
     bounds[k] = x;
+    // the sequence holding the chunk's first page (B past the last page):
+    // the decode kernel starts each chunk from it without a search
+    if (k < nchunks) cstart[k] = (x < T) ? find_range(prefix, B, x) : B;
   }
   // The sequences the combine kernel has to finish, in order: empty ones
   // (O = 0, LSE = -inf) and those cut by a chunk edge (partials to merge).
@@ -313,12 +318,12 @@ struct Seg {
 struct ChunkIter {
   const int* prefix;
   int B, k, start, end, first_page, b;
-  __device__ void init(const int* pf, const int* bounds, int B_, int k_) {
+  __device__ void init(const int* pf, const int* bounds, const int* cstart, int B_, int k_) {
     prefix = pf; B = B_; k = k_;
     start = bounds[k];
     end = bounds[k + 1];
     first_page = start;
-    b = (start < end) ? find_range(prefix, B, start) : B;
+    b = (start < end) ? cstart[k] : B;
   }
   __device__ bool next(Seg& s) {
     if (start >= end || b >= B) return false;
@@ -350,6 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const int32_t* __restrict__ seqlens, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, const int* __restrict__ hdr,
                       const int* __restrict__ prefix, const int* __restrict__ bounds,
+                      const int* __restrict__ cstart,
                       float* __restrict__ part_lse, float* __restrict__ part_o, int B,
                       int max_blocks, int num_blocks, float scale_log2, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -443,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, bounds, B, k);
+        it.init(prefix, bounds, cstart, B, k);
         Seg s;
         while (ok && it.next(s)) {
           const int L = seqlens[s.b];
@@ -550,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, bounds, B, k);
+        it.init(prefix, bounds, cstart, B, k);
         Seg s;
         while (ok && it.next(s)) {
           const int n = seg_steps(s.p0, s.p1, seqlens[s.b]);
@@ -607,7 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int total = 0;
     for (int k = cluster; k < nchunks; k += nclusters) {
       ChunkIter it;
-      it.init(prefix, bounds, B, k);
+      it.init(prefix, bounds, cstart, B, k);
       Seg s;
       while (it.next(s)) total += seg_steps(s.p0, s.p1, seqlens[s.b]);
     }
@@ -691,7 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     for (int k = cluster; k < nchunks && ok; k += nclusters) {
       ChunkIter it;
-      it.init(prefix, bounds, B, k);
+      it.init(prefix, bounds, cstart, B, k);
       Seg s;
       while (ok && it.next(s)) {
         const int L = seqlens[s.b];
@@ -1071,6 +1077,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   int* hdr = reinterpret_cast<int*>(ws + w.header);
   int* prefix = reinterpret_cast<int*>(ws + w.prefix);
   int* bounds = reinterpret_cast<int*>(ws + w.bounds);
+  int* cstart = reinterpret_cast<int*>(ws + w.cstart);
   int4* clist = reinterpret_cast<int4*>(ws + w.clist);
   float* plse = reinterpret_cast<float*>(ws + w.plse);
   float* po = reinterpret_cast<float*>(ws + w.po);
@@ -1094,7 +1101,8 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
     pc.attrs = pdl1;
     pc.numAttrs = 1;
     e = cudaLaunchKernelEx(&pc, mla_plan_kernel, (const int32_t*)a.seqlens, a.B, a.max_blocks,
-                           clusters, a.pages_per_split, hdr, prefix, bounds, clist, a.err);
+                           clusters, a.pages_per_split, hdr, prefix, bounds, cstart, clist,
+                           a.err);
     if (e != cudaSuccess) return e;
   }
   const float scale_log2 = a.scale * 1.4426950408889634f;
@@ -1114,7 +1122,8 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, mkv, mrope,
                          static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.seqlens,
                          static_cast<__nv_bfloat16*>(a.o), a.lse, (const int*)hdr,
-                         (const int*)prefix, (const int*)bounds, plse, po, a.B, a.max_blocks,
+                         (const int*)prefix, (const int*)bounds, (const int*)cstart, plse, po,
+                         a.B, a.max_blocks,
                          a.num_blocks, scale_log2, a.err);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(4 * a.num_sms, 1, 1);
