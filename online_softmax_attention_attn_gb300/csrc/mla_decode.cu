@@ -141,9 +141,10 @@ __device__ __forceinline__ int find_range(const int* __restrict__ edges, int n, 
 
 // ---- plan -------------------------------------------------------------------
 // One CTA.  Validates lengths, writes the exclusive page prefix, then the
-// chunk edges: per-sequence chunks when that is cheaper (no partials), else
-// ceil(T / clusters) pages per chunk with each cut moved to a sequence start
-// within 1/8 chunk, or a fixed split length when one is forced.
+// chunk edges, by a time model: per-sequence chunks (no partials); with fewer
+// sequences than clusters, each sequence cut into near-equal chunks of its
+// own; else ceil(T / clusters) pages per chunk with each cut moved to a
+// sequence start within 1/8 chunk; or a fixed split length when one is forced.
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restrict__ seqlens,
                                                         int B, int max_blocks, int clusters,
                                                         int pps_override, int* __restrict__ hdr,
@@ -199,9 +200,45 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     if (threadIdx.x == blockDim.x - 1) carry = incl;
     __syncthreads();
   }
+  // Fewer than half as many sequences as clusters (at most 64): each sequence
+  // may be cut into ceil(n_b / L) near-equal chunks of its own, L the shortest
+  // chunk length whose chunk count fits the clusters.  Warp 0 finds L with
+  // one sequence pair per lane; `cut` counts the chunks of cut sequences.
+  __shared__ int len3_s, n3_s, cut3_s;
+  if (threadIdx.x == 0) prefix[B] = carry;
+  __syncthreads();
+  if (wid == 0) {
+    const bool try3 = pps_override <= 0 && 2 * B <= clusters && B <= 64 && carry > 0;
+    const int n0 = (try3 && lane < B) ? prefix[lane + 1] - prefix[lane] : 0;
+    const int n1 = (try3 && lane + 32 < B) ? prefix[lane + 33] - prefix[lane + 32] : 0;
+    auto warp_sum = [&](int v) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      return v;
+    };
+    int len = 0, total = 0, cut = 0;
+    if (try3) {
+      int lo = max(1, (carry + clusters - 1) / clusters), hi = max(lo, maxn_s);
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const int t = warp_sum((n0 + mid - 1) / mid + (n1 + mid - 1) / mid);
+        if (t <= clusters) hi = mid;
+        else lo = mid + 1;
+      }
+      len = lo;
+      const int c0 = (n0 + len - 1) / len, c1 = (n1 + len - 1) / len;
+      total = warp_sum(c0 + c1);
+      cut = warp_sum((c0 > 1 ? c0 : 0) + (c1 > 1 ? c1 : 0));
+    }
+    if (lane == 0) {
+      len3_s = len;
+      n3_s = total;
+      cut3_s = cut;
+    }
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     const int T = carry;
-    prefix[B] = T;
     int mode, pps, nchunks;
     if (pps_override > 0) {
       mode = 0;
@@ -216,9 +253,21 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
       const int n_a = (T + pps - 1) / pps;
       const float est_a = fmaxf(pps * page_us, (kv + 2.f * n_a * 2.f * 262144.f) / bytes_per_us);
       const float est_b = fmaxf(maxn_s * page_us, kv / bytes_per_us);
-      if (B <= clusters && est_b <= est_a) {
+      // fewer sequences than clusters: each sequence in ceil(n_b / L) chunks
+      // of its own (no chunk spans two sequences), L the shortest chunk
+      // length whose chunk count fits the clusters; each chunk of a cut
+      // sequence writes one partial (256 KB written, then read)
+      const int len_c = len3_s, n_c = n3_s;
+      const float est_c =
+          len_c > 0 ? fmaxf(len_c * page_us, (kv + 2.f * cut3_s * 262144.f) / bytes_per_us)
+                    : 3.4e38f;
+      if (B <= clusters && est_b <= est_a && est_b <= est_c) {
         mode = 1;
         nchunks = B;
+      } else if (est_c <= est_a) {
+        mode = 3;  // the chunk edges are written by warp 0 below
+        nchunks = n_c;
+        pps = len_c;
       } else {
         mode = 2;
         nchunks = n_a;
@@ -234,7 +283,31 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   }
   __syncthreads();
   const int T = carry, mode = mode_s, pps = pps_s, nchunks = nchunks_s;
-  for (int k = threadIdx.x; k <= nchunks; k += blockDim.x) {
+  if (mode == 3 && wid == 0) {
+    // lane l writes the chunks of sequences l and l + 32, after a scan of
+    // the chunk counts gives each sequence its first chunk index
+    int first = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int b = lane + 32 * half;
+      const int n = (b < B) ? prefix[b + 1] - prefix[b] : 0;
+      const int c = (n + pps - 1) / pps;
+      int x = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      const int k0 = first + x - c;
+      for (int j = 0; j < c; ++j) {
+        bounds[k0 + j] = prefix[b] + (int)((long long)j * n / c);
+        cstart[k0 + j] = b;
+      }
+      first += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) bounds[nchunks] = T;
+  }
+  for (int k = threadIdx.x; k <= nchunks && mode != 3; k += blockDim.x) {  // 3: done above
     int x;
     if (mode == 1) {
       x = prefix[k];

@@ -178,3 +178,13 @@ def test_decode_batch_sweep_sampled(cfg):
     """The batch sweep at seq 4096: batch 16 runs through the split-KV plan
     (fewer sequences than clusters), 128 and 256 through whole chunks."""
     _sampled(cfg, 128, 3)
+
+
+def test_few_uneven_sequences_split_into_their_own_chunks():
+    """Fewer sequences than clusters with very different lengths: long ones are
+    cut into several chunks of their own, short ones stay whole, empty ones
+    are finished by the combine kernel."""
+    lens = [4096, 100, 0, 2000, 64, 1, 3000, 4096, 500, 77]
+    q, kv, table, sl = mla_inputs(len(lens), 128, lens, seed=61, paged_random=True)
+    o, lse = _gpu(q, kv, table, sl)
+    _check(q, kv, table, sl, o, lse)
