@@ -10,7 +10,8 @@ separates timed steps.  `--workload` selects another single path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload step|prefill|prefill_noncausal|decode|decode_paged|
-                              decode_b16|decode_b128|decode_b256|mla_layer|fp32|fp32_causal]
+                              decode_b16|decode_b128|decode_b256|mla_layer|fp32|fp32_causal|
+                              fp32_tc|fp32_tc_causal]
 
 Multi-GPU: the path shards into independent problems, and every box here has
 one GPU, so N ranks run N independent replicas (weak scaling); value sums
@@ -203,6 +204,27 @@ class PrefillLeg:
         return rows_flops(rows) / dt / 1e12, desc, dt
 
 
+class Tf32x3Leg(PrefillLeg):
+    """fp32 prefill on the tensor cores (three-product TF32 split): the call
+    is the split pre-pass plus the attention kernel, both inside the timing."""
+
+    def __init__(self, cfg: I.MHAConfig, dev):
+        super().__init__(cfg, dev)
+        need = self.pkg.attn_fwd_tf32x3_workspace_size(cfg.B, cfg.H, cfg.N, cfg.D)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        self.bound = "tensor_tf32"
+        self.kernel = "prefill_tf32x3_kernel"
+        self.src = ("prefill_tf32x3.cu",)
+        self.launches_per_call = 2
+
+    def run(self):
+        self.pkg.attn_fwd_tf32x3(self.dq, self.dk, self.dv, self.o, self.lse,
+                                 causal=self.cfg.causal, scale=self.cfg.scale, workspace=self.ws)
+
+    def workload_name(self):
+        return self.cfg.name + " on tensor cores (3xTF32)"
+
+
 class DecodeLeg:
     kernel = "mla_decode_kernel"
 
@@ -343,6 +365,10 @@ def make_leg(name, dev):
         return PrefillLeg(I.FP32_PAGE2, dev)
     if name == "fp32_causal":
         return PrefillLeg(I.FP32_PAGE2_CAUSAL, dev)
+    if name == "fp32_tc":
+        return Tf32x3Leg(I.FP32_PAGE2, dev)
+    if name == "fp32_tc_causal":
+        return Tf32x3Leg(I.FP32_PAGE2_CAUSAL, dev)
     if name == "decode":
         return DecodeLeg(I.MLA_B64, dev)
     if name == "decode_paged":
@@ -437,9 +463,11 @@ def make_leg_cpu(name):
             self.q, self.kv, self.table, self.sl = I.mla_config_inputs(cfg)
             self.bytes = metrics.mla_bytes(self.sl.tolist(), cfg.Hq,
                                            max_blocks=self.table.shape[1])
-    if name in ("prefill", "prefill_noncausal", "fp32", "fp32_causal"):
+    if name in ("prefill", "prefill_noncausal", "fp32", "fp32_causal", "fp32_tc",
+                "fp32_tc_causal"):
         cfg = {"prefill": I.BF16_PREFILL, "prefill_noncausal": I.BF16_PREFILL_NONCAUSAL,
-               "fp32": I.FP32_PAGE2, "fp32_causal": I.FP32_PAGE2_CAUSAL}[name]
+               "fp32": I.FP32_PAGE2, "fp32_causal": I.FP32_PAGE2_CAUSAL,
+               "fp32_tc": I.FP32_PAGE2, "fp32_tc_causal": I.FP32_PAGE2_CAUSAL}[name]
         return _P(cfg)
     return _D(I.MLA_B64 if name == "decode" else I.MLA_B256_PAGED)
 
@@ -469,7 +497,7 @@ def main():
     ap.add_argument("--workload", default="step",
                     choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged",
                              "decode_b16", "decode_b128", "decode_b256", "mla_layer", "fp32",
-                             "fp32_causal"])
+                             "fp32_causal", "fp32_tc", "fp32_tc_causal"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -560,7 +588,7 @@ def main():
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if main_leg.bound != "alu" else "f32", "data": "synthetic",
+        "dtype": "bf16" if main_leg.bound in ("tensor", "hbm") else "f32", "data": "synthetic",
         "config": config_of(args.workload, main_leg),
         "wall_ms_per_step": wall_max / args.steps * 1e3,
     }
@@ -569,6 +597,16 @@ def main():
         peak = peaks.get("bf16_tflops")
         achieved = main_leg.flops / (main_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
+    elif main_leg.bound == "tensor_tf32":
+        # tf32 dense peak: the measured bf16 peak x the nominal tf32 / bf16
+        # ratio (1.1 / 2.25 PFLOP/s); three MMAs per product cap frac at 1/3
+        peak = peaks.get("bf16_tflops") * (1.1 / 2.25)
+        achieved = main_leg.flops / (main_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "peak_dtype": "tf32 (measured bf16 x 1.1/2.25)", "mma_per_product": 3}
+        props = torch.cuda.get_device_properties(dev)
+        smax = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+        roof["ffma_peak"] = props.multi_processor_count * 128 * 2 * smax * 1e6 / 1e12
     elif main_leg.bound == "hbm":
         peak = peaks.get("hbm_gbs")
         achieved = main_leg.bytes / (main_ms * 1e-3) / 1e9
@@ -627,7 +665,7 @@ def _leg_works(leg, pkg):
 
 def _launches(leg, pkg):
     if isinstance(leg, PrefillLeg):
-        return 1
+        return getattr(leg, "launches_per_call", 1)
     return 3  # plan, decode, combine
 
 

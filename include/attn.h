@@ -90,6 +90,45 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              void* stream);
 
 /*
+ * attn_fwd_tf32x3_workspace_size -- bytes of device workspace that
+ * attn_fwd_tf32x3 needs for (B, H, N, D): 2 x B*H*N*64 floats for the split
+ * K (each part rounded up to 256 bytes) plus 2 x B*H*64*Np floats for the
+ * split, transposed V (Np = N rounded up to a multiple of 64).  Returns 0 for
+ * invalid sizes or D != 64.  Pure host arithmetic: no CUDA call.
+ */
+ATTN_API size_t attn_fwd_tf32x3_workspace_size(int B, int H, int N, int D);
+
+/*
+ * attn_fwd_tf32x3 -- fp32 attention forward on the tensor cores, accurate to
+ * fp32 level: the same operation as attn_fwd with ATTN_DTYPE_F32 (the fp32
+ * FlashAttention-2 forward of the "FP32 CUDA-core FlashAttention-2 v2" blog,
+ * sections 1.2-1.4 and 3.3-3.5, with the tensor cores of its section 5 list
+ * of what is left to do).  Every fp32 operand x is split into
+ * hi = tf32(x) and lo = tf32(x - hi), and every product is taken as
+ * lo*hi + hi*lo + hi*hi on tcgen05 kind::tf32 with fp32 accumulation.
+ *
+ *   q, k, v : [B, H, N, 64] float32, contiguous.
+ *   o       : [B, H, N, 64] float32 (written).
+ *   lse     : [B, H, N] float32 (written), as for attn_fwd.
+ *   causal, scale : as for attn_fwd.
+ *   workspace : device buffer of >= attn_fwd_tf32x3_workspace_size(B, H, N, D)
+ *             bytes, owned by the caller; the call overwrites it (a split
+ *             copy of K and a split, transposed copy of V) and it must not be
+ *             used by another call that is in flight at the same time.
+ *   stream  : cudaStream_t or NULL.
+ * Two kernels are enqueued: the split pre-pass, then the attention kernel
+ * as a programmatic dependent of it.  Nothing is allocated.
+ * Requirements: pointers non-null and 16-byte aligned; B, H, N >= 1; D = 64;
+ * B*H*N < 2^31.
+ * Errors: INVALID_ARG (null, size <= 0, non-finite scale), UNSUPPORTED
+ * (D != 64, too large), MISALIGNED, WORKSPACE_TOO_SMALL, CUDA.  A stuck
+ * pipeline is reported later by attn_device_status as DEVICE_TIMEOUT.
+ */
+ATTN_API int attn_fwd_tf32x3(const float* q, const float* k, const float* v, float* o,
+                    float* lse, int B, int H, int N, int D, int causal, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode needs.
  *
  *   B, Hq, max_blocks_per_seq : as for mla_decode.

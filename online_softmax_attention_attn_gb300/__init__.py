@@ -7,6 +7,9 @@ or cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   attn_fwd(q, k, v, o=None, lse=None, causal=False, scale=None, stream=None)
+  attn_fwd_tf32x3(q, k, v, o=None, lse=None, causal=False, scale=None,
+                  workspace=None, stream=None)
+  attn_fwd_tf32x3_workspace_size(B, H, N, D)
   mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None, scale=...,
              workspace=None, stream=None)
   mla_decode_split(..., pages_per_split=...)
@@ -21,7 +24,8 @@ import math
 import os
 
 __all__ = [
-    "AttnError", "lib", "attn_fwd", "mla_decode", "mla_decode_split",
+    "AttnError", "lib", "attn_fwd", "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size",
+    "mla_decode", "mla_decode_split",
     "mla_decode_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
     "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
@@ -70,6 +74,11 @@ def lib():
         L.attn_fwd_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                               _f, _vp, _i]
         L.attn_fwd_test_skip_load.restype = _i
+        L.attn_fwd_tf32x3_workspace_size.argtypes = [_i, _i, _i, _i]
+        L.attn_fwd_tf32x3_workspace_size.restype = _sz
+        L.attn_fwd_tf32x3.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp,
+                                      _sz, _vp]
+        L.attn_fwd_tf32x3.restype = _i
         L.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
         L.mla_decode_workspace_size.restype = _sz
         L.mla_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp, _sz,
@@ -155,6 +164,39 @@ def attn_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | Non
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
                           int(bool(causal)), scale, code, _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_fwd_tf32x3_workspace_size(B: int, H: int, N: int, D: int = 64) -> int:
+    return int(lib().attn_fwd_tf32x3_workspace_size(B, H, N, D))
+
+
+def attn_fwd_tf32x3(q, k, v, o=None, lse=None, causal: bool = False,
+                    scale: float | None = None, workspace=None, stream=None):
+    """fp32 attention forward on the tensor cores (three-product TF32 split).
+
+    q, k, v: [B,H,N,64] float32 CUDA tensors.  Returns (o, lse) as attn_fwd.
+    `workspace` (uint8, >= attn_fwd_tf32x3_workspace_size bytes) is allocated
+    when not given.
+    """
+    import torch
+    B, H, N, D = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, torch.float32, (B, H, N, D))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    _require(o, "o", torch.float32, (B, H, N, D))
+    _require(lse, "lse", torch.float32, (B, H, N))
+    if workspace is None:
+        need = attn_fwd_tf32x3_workspace_size(B, H, N, D)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _require(workspace, "workspace", torch.uint8)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().attn_fwd_tf32x3(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                                 int(bool(causal)), scale, _ptr(workspace), workspace.numel(),
+                                 _stream_ptr(stream)))
     return o, lse
 
 

@@ -160,6 +160,42 @@ extern "C" int attn_fwd_test_skip_load(const void* q, const void* k, const void*
                        skip_load_index);
 }
 
+// ------------------------------------------------------- attn_fwd_tf32x3
+
+extern "C" size_t attn_fwd_tf32x3_workspace_size(int B, int H, int N, int D) {
+  if (B <= 0 || H <= 0 || N <= 0 || D != 64) return 0;
+  return prefill_tf32x3_workspace_bytes(B, H, N);
+}
+
+extern "C" int attn_fwd_tf32x3(const float* q, const float* k, const float* v, float* o,
+                               float* lse, int B, int H, int N, int D, int causal, float scale,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = '\0';
+  if (!q || !k || !v || !o || !lse || !workspace)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_tf32x3: null pointer argument");
+  if (B <= 0 || H <= 0 || N <= 0 || D <= 0)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "attn_fwd_tf32x3: B, H, N, D must be >= 1 (got %d %d %d %d)", B, H, N, D);
+  if (!isfinite(scale))
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_tf32x3: scale is not finite");
+  if (D != 64) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_tf32x3: built for D=64 (got %d)", D);
+  if ((long long)B * H * N > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_tf32x3: B*H*N exceeds the tensor-map range");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return fail(ATTN_ERR_MISALIGNED, "attn_fwd_tf32x3: pointers must be 16-byte aligned");
+  const size_t need = prefill_tf32x3_workspace_bytes(B, H, N);
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE_TOO_SMALL, "attn_fwd_tf32x3: workspace %zu < %zu bytes",
+                workspace_bytes, need);
+  int code = ATTN_OK;
+  int* err = device_err_word(&code);
+  if (!err) return code;
+  PrefillTf32x3Args a{q, k, v, o, lse, B, H, N, D, causal != 0, scale, workspace, err};
+  return finish_launch(launch_prefill_tf32x3(a, static_cast<cudaStream_t>(stream)),
+                       "attn_fwd_tf32x3");
+}
+
 // ---------------------------------------------------------------- MLA
 
 extern "C" size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_seq,

@@ -96,6 +96,19 @@ struct PrefillBf16Args {
   int debug_skip_load;  // test hook: >0 skips that K/V load (bounded-wait test)
 };
 
+struct PrefillTf32x3Args {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;
+  float* lse;
+  int B, H, N, D;
+  int causal;
+  float scale;
+  void* workspace;  // >= prefill_tf32x3_workspace_bytes(B, H, N)
+  int* err;
+};
+
 struct MlaArgs {
   const void* q;
   const void* kv;
@@ -119,11 +132,14 @@ struct MlaArgs {
 cudaError_t launch_prefill_f32(const PrefillF32Args& a, cudaStream_t s);
 cudaError_t launch_prefill_bf16(const PrefillBf16Args& a, cudaStream_t s);
 cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_tf32x3(const PrefillTf32x3Args& a, cudaStream_t s);
 
 // Kernel shape queries (host-only, no CUDA calls).
 bool prefill_f32_info(int D, int* Br, int* Bc, int* threads, int* smem);
 bool prefill_bf16_info(int D, int* Br, int* Bc, int* threads, int* smem);
 size_t mla_workspace_bytes(int B, int Hq, int max_blocks, int num_sms, int pages_per_split);
+size_t prefill_tf32x3_workspace_bytes(int B, int H, int N);
+bool prefill_tf32x3_info(int* Br, int* Bc, int* threads, int* smem);
 
 // Fixed-scratch support for mla_decode_noalloc (defined in mla_decode.cu).
 cudaError_t mla_noalloc_scratch(void** ptr, size_t* bytes);

@@ -341,6 +341,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          ((uint32_t)(M >> 4) << 24);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::tf32 (tf32 in 32-bit containers,
+// fp32 accumulate).  A in TMEM holds one element per 32-bit column.
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::tf32: tf32 A and B (format 2), fp32 D, dense,
+// both operands K-major.  Same fields as idesc_bf16.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start>>4, 16-29 leading byte offset>>4, 32-45 stride byte
 //   offset>>4, 46-48 fixed 0b001, 49-51 base offset (0: atoms 1024-B aligned),

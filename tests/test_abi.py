@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
               "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
-              "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out"]:
+              "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out",
+              "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size"]:
         assert n in names
 
 
@@ -116,3 +117,26 @@ def test_projection_arguments_are_checked_before_any_cuda_call(L):
     odd = ctypes.c_void_p(aligned.value + 2)
     rc = L.mla_project_out(odd, aligned, aligned, 4, 128, 512, 128, None)
     assert rc == pkg.ATTN_ERR_MISALIGNED
+
+
+def test_tf32x3_workspace_and_argument_checks(L):
+    """attn_fwd_tf32x3: workspace arithmetic and host-side rejections."""
+    # split K: 2 x BH*N*64 floats; split V^T: 2 x BH*64*ceil64(N) floats
+    assert pkg.attn_fwd_tf32x3_workspace_size(4, 8, 8192, 64) == 4 * 32 * 8192 * 64 * 4
+    assert pkg.attn_fwd_tf32x3_workspace_size(1, 2, 100, 64) == \
+        2 * 2 * 100 * 256 + 2 * 2 * 64 * 128 * 4
+    assert pkg.attn_fwd_tf32x3_workspace_size(1, 1, 16, 128) == 0
+    assert pkg.attn_fwd_tf32x3_workspace_size(0, 1, 16, 64) == 0
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    rc = L.attn_fwd_tf32x3(None, p, p, p, p, 1, 1, 16, 64, 0, 0.1, p, 1 << 20, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG and "null" in pkg.attn_last_error()
+    rc = L.attn_fwd_tf32x3(p, p, p, p, p, 1, 1, 16, 64, 0, float("nan"), p, 1 << 20, None)
+    assert rc == pkg.ATTN_ERR_INVALID_ARG
+    rc = L.attn_fwd_tf32x3(p, p, p, p, p, 1, 1, 16, 128, 0, 0.1, p, 1 << 20, None)
+    assert rc == pkg.ATTN_ERR_UNSUPPORTED
+    rc = L.attn_fwd_tf32x3(p, p, p, p, ctypes.c_void_p(20), 1, 1, 16, 64, 0, 0.1, p, 1 << 20,
+                           None)
+    assert rc == pkg.ATTN_ERR_MISALIGNED
+    need = pkg.attn_fwd_tf32x3_workspace_size(1, 1, 16, 64)
+    rc = L.attn_fwd_tf32x3(p, p, p, p, p, 1, 1, 16, 64, 0, 0.1, p, need - 1, None)
+    assert rc == pkg.ATTN_ERR_WORKSPACE_TOO_SMALL
