@@ -17,20 +17,23 @@
 // rounding of lo being below 2^-21 |x*y|.  Every product of the kernel (Q K^T
 // and P V) is three tcgen05.mma kind::tf32 into the same fp32 accumulator.
 //
-// Layout and roles (one Q tile of 128 rows per CTA, 192 threads):
+// Layout and roles (one Q tile of 128 rows per CTA, 224 threads):
 //   * pre-pass (tf32x3_split_kernel): K -> K_hi, K_lo ([BH, N, 64]) and
 //     V -> V^T_hi, V^T_lo ([BH, 64, Np], Np = N rounded up to 64, tail keys
 //     zero) in a caller workspace, once per call, so that every MMA operand
 //     is K-major (the keys are the contraction dimension of P V).
 //   * warp 4 : TMA producer.  K_hi, K_lo, V^T_hi, V^T_lo of one 64-key block
 //     form one 64 KB stage (128-byte swizzle, 32-float atoms); 3 stages.
-//   * warp 5 : MMA issuer (one thread) and TMEM owner.
+//   * warp 6 : S issuer (one thread).
 //       S_j = Q K_j^T : A = Q_hi / Q_lo from TMEM, B = K_hi / K_lo (smem),
-//                       M=128 N=64, 8 k-steps of 8 x 3 products.
+//                       M=128 N=64, 8 k-steps of 8 x 3 products,
+//     into buffer j&1 once PV_{j-2} (the last reader of that buffer) is done.
+//   * warp 5 : PV issuer (one thread) and TMEM owner.
 //       O += P_j V_j  : A = P_hi / P_lo from TMEM, B = V^T_hi / V^T_lo,
 //                       M=128 N=64, 8 k-steps of 8 x 3 products.
-//     Issue order S_0, S_1, PV_0, S_2, PV_1, S_3, ...: two S buffers keep the
-//     tensor core busy while the softmax of the other block runs.
+//     Two S buffers keep the tensor core busy while the softmax of the other
+//     block runs; two issuing threads in different warps keep the pipe fed
+//     (one thread alone is paced by its own issue cost, not by the pipe).
 //   * warps 0-3 : softmax, one thread per query row (TMEM lane = row).  They
 //     split the row's Q into TMEM, then per block: S -> scale, mask, running
 //     max (lazy: O and l are rescaled only when the max grew by more than
@@ -52,7 +55,7 @@ using namespace gb300;
 constexpr int kD = 64;
 constexpr int kBM = 128;               // query rows per CTA
 constexpr int kBN = 64;                // keys per KV block
-constexpr int kThreads = 192;          // 4 softmax warps, producer, MMA
+constexpr int kThreads = 224;          // 4 softmax warps, producer, PV issuer, S issuer
 constexpr int kAtomBytes = 64 * 128;   // 64 rows x 32 floats (one 128-byte swizzle column)
 constexpr int kPartBytes = 2 * kAtomBytes;  // one 64 x 64 fp32 operand block
 constexpr int kStageBytes = 4 * kPartBytes; // K_hi, K_lo, V^T_hi, V^T_lo
@@ -62,9 +65,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kRingOff = 0;
 constexpr int kBarOff = kRingOff + kStages * kStageBytes;
 // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2],
-// pv_done[2], mma_drain.  The two-buffer barriers complete once every other
-// block, so no waiter is ever two of their phases behind or ahead.
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+// pv_done[2], pv_drain, s_drain.  The two-buffer barriers complete once every
+// other block, so no waiter is ever two of their phases behind or ahead.
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -164,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_s_full = [&](int b) { return bar0 + 8u * (1 + 2 * kStages + b); };
   auto bar_p_full = [&](int b) { return bar0 + 8u * (3 + 2 * kStages + b); };
   auto bar_pv_done = [&](int b) { return bar0 + 8u * (5 + 2 * kStages + b); };
-  const uint32_t bar_mma_drain = bar0 + 8u * (7 + 2 * kStages);
+  const uint32_t bar_pv_drain = bar0 + 8u * (7 + 2 * kStages);
+  const uint32_t bar_s_drain = bar0 + 8u * (8 + 2 * kStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -191,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_p_full(b), 128);
       mbar_init(bar_pv_done(b), 1);
     }
-    mbar_init(bar_mma_drain, 1);
+    mbar_init(bar_pv_drain, 1);
+    mbar_init(bar_s_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmKhi);
@@ -248,70 +253,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ================= MMA issuer =================
+  } else if (warp == 5 || warp == 6) {
+    // ================= MMA issuers: PV (warp 5), S (warp 6) =================
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_tf32(kBM, 64);
       // K-major operands, 128-byte rows of 32 floats in 8-row groups 1024 B
       // apart; a k-step of 8 floats is 32 B inside the atom, the second half
       // of the 64-wide contraction is the next atom.
       const uint64_t d0 = sdesc_sw128(sRing, 16, 1024);
-      bool ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
-      if (ok) tc_fence_after();
-
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kStages;
-        if (!mbar_wait(bar_kv_full(s), (j / kStages) & 1, abort_flag, err, kSiteKvFull, j))
-          return false;
-        tc_fence_after();
-        const uint32_t dS = tbase + kColS + 128u * (j & 1);
-        const uint64_t khi = d0 + (uint64_t)((s * kStageBytes) >> 4);
-        const uint64_t klo = khi + (uint64_t)(kPartBytes >> 4);
+      bool ok = true;
+      if (warp == 6) {
+        ok = mbar_wait(bar_q_full, 0, abort_flag, err, kSiteQFull, 0);
+        for (int j = 0; j < T && ok; ++j) {
+          const int s = j % kStages;
+          // buffer j&1 was last read by PV_{j-2}
+          if (j >= 2)
+            ok = mbar_wait(bar_pv_done(j & 1), ((j - 2) >> 1) & 1, abort_flag, err,
+                           kSitePvDone, j);
+          if (ok) ok = mbar_wait(bar_kv_full(s), (j / kStages) & 1, abort_flag, err,
+                                 kSiteKvFull, j);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dS = tbase + kColS + 128u * (j & 1);
+          const uint64_t khi = d0 + (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t klo = khi + (uint64_t)(kPartBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kD / 8; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-          mma_ts_tf32(dS, tbase + kColQlo + 8 * kk, khi + off, kIdesc, kk > 0);
-          mma_ts_tf32(dS, tbase + kColQhi + 8 * kk, klo + off, kIdesc, 1u);
-          mma_ts_tf32(dS, tbase + kColQhi + 8 * kk, khi + off, kIdesc, 1u);
+          for (int kk = 0; kk < kD / 8; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+            mma_ts_tf32(dS, tbase + kColQlo + 8 * kk, khi + off, kIdesc, kk > 0);
+            mma_ts_tf32(dS, tbase + kColQhi + 8 * kk, klo + off, kIdesc, 1u);
+            mma_ts_tf32(dS, tbase + kColQhi + 8 * kk, khi + off, kIdesc, 1u);
+          }
+          tc_commit(bar_s_full(j & 1));
         }
-        tc_commit(bar_s_full(j & 1));
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int b = j & 1;
-        if (!mbar_wait(bar_p_full(b), (j >> 1) & 1, abort_flag, err, kSitePFull, j))
-          return false;
-        tc_fence_after();
-        const int s = j % kStages;
-        const uint64_t vhi = d0 + (uint64_t)((s * kStageBytes + 2 * kPartBytes) >> 4);
-        const uint64_t vlo = vhi + (uint64_t)(kPartBytes >> 4);
-        const uint32_t aPhi = tbase + kColS + 128u * b;
-        const uint32_t aPlo = aPhi + 64;
-        const uint32_t dO = tbase + kColO;
+        // every MMA this thread issued must be complete before TMEM is freed
+        tc_commit(bar_s_drain);
+        volatile int never = 0;
+        mbar_wait(bar_s_drain, 0, &never, nullptr, kSiteDrain, -3);
+      } else {
+        for (int j = 0; j < T && ok; ++j) {
+          const int b = j & 1;
+          ok = mbar_wait(bar_p_full(b), (j >> 1) & 1, abort_flag, err, kSitePFull, j);
+          if (!ok) break;
+          tc_fence_after();
+          const int s = j % kStages;
+          const uint64_t vhi = d0 + (uint64_t)((s * kStageBytes + 2 * kPartBytes) >> 4);
+          const uint64_t vlo = vhi + (uint64_t)(kPartBytes >> 4);
+          const uint32_t aPhi = tbase + kColS + 128u * b;
+          const uint32_t aPlo = aPhi + 64;
+          const uint32_t dO = tbase + kColO;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 8; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-          mma_ts_tf32(dO, aPlo + 8 * kk, vhi + off, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_ts_tf32(dO, aPhi + 8 * kk, vlo + off, kIdesc, 1u);
-          mma_ts_tf32(dO, aPhi + 8 * kk, vhi + off, kIdesc, 1u);
+          for (int kk = 0; kk < kBN / 8; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+            mma_ts_tf32(dO, aPlo + 8 * kk, vhi + off, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_tf32(dO, aPhi + 8 * kk, vlo + off, kIdesc, 1u);
+            mma_ts_tf32(dO, aPhi + 8 * kk, vhi + off, kIdesc, 1u);
+          }
+          tc_commit(bar_pv_done(b));
+          // S_j completed before P_j existed, so PV_j is the stage's last reader
+          tc_commit(bar_kv_empty(s));
         }
-        tc_commit(bar_pv_done(b));
-        tc_commit(bar_kv_empty(s));  // S_j and PV_j were the stage's readers
-        return true;
-      };
-
-      if (ok) ok = issue_s(0);
-      if (ok && T > 1) ok = issue_s(1);
-      for (int j = 0; j < T && ok; ++j) {
-        ok = issue_pv(j);
-        // S_{j+2} reuses buffer j&1: PV_j, issued before it by this thread,
-        // has read P_j from it by then (tcgen05 MMAs of one thread run in order)
-        if (ok && j + 2 < T) ok = issue_s(j + 2);
+        tc_commit(bar_pv_drain);
+        volatile int never = 0;
+        mbar_wait(bar_pv_drain, 0, &never, nullptr, kSiteDrain, -2);
       }
-      // every MMA this thread issued must be complete before TMEM is freed
-      tc_commit(bar_mma_drain);
-      volatile int never = 0;
-      mbar_wait(bar_mma_drain, 0, &never, nullptr, kSiteDrain, -2);
     }
     __syncwarp();
   } else {
