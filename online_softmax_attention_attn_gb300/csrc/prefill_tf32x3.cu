@@ -14,23 +14,31 @@
 // bits, too few for a 1e-4 bound on O.  Each fp32 operand x is written as
 // x = hi + lo with hi = x rounded to TF32 and lo = (x - hi) rounded to TF32;
 // then x*y ~ lo_x*hi_y + hi_x*lo_y + hi_x*hi_y, the dropped lo_x*lo_y and the
-// rounding of lo being below 2^-21 |x*y|.  Every product of the kernel (Q K^T
-// and P V) is three tcgen05.mma kind::tf32 into the same fp32 accumulator.
+// rounding of lo being below 2^-21 |x*y|.  Q K^T is three tcgen05.mma
+// kind::tf32 into one fp32 accumulator.  In P V the two cross terms carry
+// only 2^-11 of the product, so they run as kind::f16 MMAs on bf16 operands
+// (bf16(P_lo) bf16(V) + bf16(P) bf16(V_lo), 16 keys per MMA instead of 8)
+// into the same fp32 accumulator: their bf16 rounding costs below 2^-19 of
+// each product, against a bound of 1e-4 on O, and P V needs 16 MMAs per
+// block instead of 24.
 //
 // Layout and roles (one Q tile of 128 rows per CTA, 224 threads):
-//   * pre-pass (tf32x3_split_kernel): K -> K_hi, K_lo ([BH, N, 64]) and
-//     V -> V^T_hi, V^T_lo ([BH, 64, Np], Np = N rounded up to 64, tail keys
-//     zero) in a caller workspace, once per call, so that every MMA operand
-//     is K-major (the keys are the contraction dimension of P V).
-//   * warp 4 : TMA producer.  K_hi, K_lo, V^T_hi, V^T_lo of one 64-key block
-//     form one 64 KB stage (128-byte swizzle, 32-float atoms); 3 stages.
+//   * pre-pass (tf32x3_split_kernel): K -> K_hi, K_lo ([BH, N, 64] fp32) and
+//     V -> V^T_hi (fp32), bf16(V)^T and bf16(V_lo)^T ([BH, 64, Np], Np = N
+//     rounded up to 64, tail keys zero) in a caller workspace, once per call,
+//     so that every MMA operand is K-major (the keys are the contraction
+//     dimension of P V).
+//   * warp 4 : TMA producer.  K_hi, K_lo, V^T_hi (16 KB each) and the two
+//     bf16 V^T tiles (8 KB each) of one 64-key block form one 64 KB stage
+//     (128-byte swizzle); 3 stages.
 //   * warp 6 : S issuer (one thread).
 //       S_j = Q K_j^T : A = Q_hi / Q_lo from TMEM, B = K_hi / K_lo (smem),
 //                       M=128 N=64, 8 k-steps of 8 x 3 products,
 //     into buffer j&1 once PV_{j-2} (the last reader of that buffer) is done.
 //   * warp 5 : PV issuer (one thread) and TMEM owner.
-//       O += P_j V_j  : A = P_hi / P_lo from TMEM, B = V^T_hi / V^T_lo,
-//                       M=128 N=64, 8 k-steps of 8 x 3 products.
+//       O += P_j V_j  : hi x hi: A = P_hi (tf32, TMEM), B = V^T_hi, 8 k-steps
+//                       of 8; cross terms: A = bf16(P_lo) / bf16(P) (TMEM),
+//                       B = bf16(V)^T / bf16(V_lo)^T, 4 k-steps of 16 x 2.
 //     Two S buffers keep the tensor core busy while the softmax of the other
 //     block runs; two issuing threads in different warps keep the pipe fed
 //     (one thread alone is paced by its own issue cost, not by the pipe).
@@ -38,10 +46,12 @@
 //     split the row's Q into TMEM, then per block: S -> scale, mask, running
 //     max (lazy: O and l are rescaled only when the max grew by more than
 //     2^8, exact because both share the stale reference), P = 2^(t - m),
-//     row sum, P_hi over the S columns and P_lo beside them.  Epilogue:
+//     row sum, P_hi over the S columns, bf16(P) and bf16(P_lo) beside them.
+//     Epilogue:
 //     O / l (fp32) and LSE straight to global memory.
 //   TMEM columns: Q_hi [0,64), Q_lo [64,128), O [128,192),
-//   buffer b: S / P_hi [256+128b, +64), P_lo [320+128b, +64).
+//   buffer b: S / P_hi [256+128b, +64), bf16(P) [320+128b, +32),
+//   bf16(P_lo) [352+128b, +32) (two bf16 per column).
 //   Every wait is bounded (about 2 s); a stuck pipeline records
 //   ATTN_ERR_DEVICE_TIMEOUT and the CTA unwinds, frees TMEM and exits.
 #include <math.h>
@@ -56,9 +66,11 @@ constexpr int kD = 64;
 constexpr int kBM = 128;               // query rows per CTA
 constexpr int kBN = 64;                // keys per KV block
 constexpr int kThreads = 224;          // 4 softmax warps, producer, PV issuer, S issuer
-constexpr int kAtomBytes = 64 * 128;   // 64 rows x 32 floats (one 128-byte swizzle column)
+constexpr int kAtomBytes = 64 * 128;   // 64 rows x 128 B (one 128-byte swizzle column)
 constexpr int kPartBytes = 2 * kAtomBytes;  // one 64 x 64 fp32 operand block
-constexpr int kStageBytes = 4 * kPartBytes; // K_hi, K_lo, V^T_hi, V^T_lo
+constexpr int kVbOff = 3 * kPartBytes;      // bf16(V)^T: one atom (64 rows x 64 bf16)
+constexpr int kVlbOff = kVbOff + kAtomBytes;  // bf16(V_lo)^T
+constexpr int kStageBytes = kVlbOff + kAtomBytes;  // K_hi, K_lo, V^T_hi, two bf16 V^T
 constexpr int kStages = 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -74,7 +86,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQhi = 0;
 constexpr uint32_t kColQlo = 64;
 constexpr uint32_t kColO = 128;
-constexpr uint32_t kColS = 256;    // + 128 * buffer; P_lo at + 64
+constexpr uint32_t kColS = 256;    // + 128 * buffer; bf16(P) at + 64, bf16(P_lo) at + 96
 
 // Round to the TF32 grid (10 explicit mantissa bits), to nearest with ties
 // away from zero: add half a TF32 unit to the magnitude bits and clear the 13
@@ -86,7 +98,8 @@ __device__ __forceinline__ float tf32_round(float x) {
 // ------------------------------------------------------------ pre-pass
 
 // One block per 64 keys, looping over heads: K rows are split in place of
-// layout, V rows split and transposed through shared memory.  Keys in
+// layout, V rows split (V_hi in fp32, V and V - V_hi in bf16) and transposed
+// through shared memory.  Keys in
 // [N, Np) of V^T are written as zeros (their P is 0, and 0 * garbage could
 // be NaN); K rows past N are never read (the tensor map ends at N).
 __device__ __forceinline__ void split4(float4 x, float4& h, float4& l) {
@@ -99,8 +112,8 @@ __device__ __forceinline__ void split4(float4 x, float4& h, float4& l) {
 __global__ void __launch_bounds__(256)
     tf32x3_split_kernel(const float* __restrict__ k, const float* __restrict__ v,
                         float* __restrict__ k_hi, float* __restrict__ k_lo,
-                        float* __restrict__ vt_hi, float* __restrict__ vt_lo, int N, int Np,
-                        int BH) {
+                        float* __restrict__ vt_hi, __nv_bfloat16* __restrict__ vt_b,
+                        __nv_bfloat16* __restrict__ vt_lo_b, int N, int Np, int BH) {
   __shared__ float tile[64][kD + 1];
   // the attention kernel may be scheduled now; it waits for this grid's
   // completion before its first read of the split operands
@@ -137,7 +150,11 @@ __global__ void __launch_bounds__(256)
       split4(x, h, l);
       const size_t off = vt_base + (size_t)d * Np + key0 + 4 * k4;
       *reinterpret_cast<float4*>(vt_hi + off) = h;
-      *reinterpret_cast<float4*>(vt_lo + off) = l;
+      // the cross terms' bf16 operands: V itself and V - V_hi
+      *reinterpret_cast<uint2*>(vt_b + off) =
+          make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+      *reinterpret_cast<uint2*>(vt_lo_b + off) = make_uint2(
+          pack_bf16x2(x.x - h.x, x.y - h.y), pack_bf16x2(x.z - h.z, x.w - h.w));
     }
     __syncthreads();  // the tile is refilled for the next head
   }
@@ -150,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tf32x3_kernel(const __grid_constant__ CUtensorMap tmKhi,
                           const __grid_constant__ CUtensorMap tmKlo,
                           const __grid_constant__ CUtensorMap tmVhi,
-                          const __grid_constant__ CUtensorMap tmVlo,
+                          const __grid_constant__ CUtensorMap tmVb,
+                          const __grid_constant__ CUtensorMap tmVlb,
                           const float* __restrict__ q, float* __restrict__ o,
                           float* __restrict__ lse, int BH, int N, float scale_log2, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -202,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmKhi);
     prefetch_tmap(&tmKlo);
     prefetch_tmap(&tmVhi);
-    prefetch_tmap(&tmVlo);
+    prefetch_tmap(&tmVb);
+    prefetch_tmap(&tmVlb);
   }
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -238,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pol);
           tma_load_3d_hint(dst + 2 * kPartBytes + a * kAtomBytes, &tmVhi, bar, j * kBN + 32 * a,
                            0, bh, pol);
-          tma_load_3d_hint(dst + 3 * kPartBytes + a * kAtomBytes, &tmVlo, bar, j * kBN + 32 * a,
-                           0, bh, pol);
         }
+        tma_load_3d_hint(dst + kVbOff, &tmVb, bar, j * kBN, 0, bh, pol);
+        tma_load_3d_hint(dst + kVlbOff, &tmVlb, bar, j * kBN, 0, bh, pol);
       }
       if (!ok) {
         // let every copy this thread started land before the CTA unwinds
@@ -257,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= MMA issuers: PV (warp 5), S (warp 6) =================
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_tf32(kBM, 64);
+      constexpr uint32_t kIdescB = idesc_bf16(kBM, 64, false, false);
       // K-major operands, 128-byte rows of 32 floats in 8-row groups 1024 B
       // apart; a k-step of 8 floats is 32 B inside the atom, the second half
       // of the 64-wide contraction is the next atom.
@@ -298,15 +318,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int s = j % kStages;
           const uint64_t vhi = d0 + (uint64_t)((s * kStageBytes + 2 * kPartBytes) >> 4);
-          const uint64_t vlo = vhi + (uint64_t)(kPartBytes >> 4);
+          const uint64_t vb = d0 + (uint64_t)((s * kStageBytes + kVbOff) >> 4);
+          const uint64_t vlb = d0 + (uint64_t)((s * kStageBytes + kVlbOff) >> 4);
           const uint32_t aPhi = tbase + kColS + 128u * b;
-          const uint32_t aPlo = aPhi + 64;
+          const uint32_t aPb = aPhi + 64;
+          const uint32_t aPlb = aPhi + 96;
           const uint32_t dO = tbase + kColO;
+          // cross terms first (bf16, 16 keys = 8 columns = 32 B per k-step)
+#pragma unroll
+          for (int kb = 0; kb < kBN / 16; ++kb) {
+            const uint64_t off = (uint64_t)((kb * 32) >> 4);
+            mma_ts(dO, aPlb + 8 * kb, vb + off, kIdescB, (j > 0 || kb > 0) ? 1u : 0u);
+            mma_ts(dO, aPb + 8 * kb, vlb + off, kIdescB, 1u);
+          }
 #pragma unroll
           for (int kk = 0; kk < kBN / 8; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-            mma_ts_tf32(dO, aPlo + 8 * kk, vhi + off, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_ts_tf32(dO, aPhi + 8 * kk, vlo + off, kIdesc, 1u);
             mma_ts_tf32(dO, aPhi + 8 * kk, vhi + off, kIdesc, 1u);
           }
           tc_commit(bar_pv_done(b));
@@ -396,19 +423,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         r0 += sv[c]; r1 += sv[c + 1]; r2 += sv[c + 2]; r3 += sv[c + 3];
       }
       l += (r0 + r1) + (r2 + r3);
-      // P_hi over the S columns, P_lo beside them
+      // P_hi (tf32) over the S columns; bf16(P) and bf16(P - P_hi) beside them
+      {
+        uint32_t pb[32], plb[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t hi[32], lo[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t hi[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float x = sv[32 * h + u];
-          const float xh = tf32_round(x);
-          hi[u] = __float_as_uint(xh);
-          lo[u] = __float_as_uint(tf32_round(x - xh));
+          for (int u = 0; u < 32; u += 2) {
+            const float x0 = sv[32 * h + u], x1 = sv[32 * h + u + 1];
+            const float h0 = tf32_round(x0), h1 = tf32_round(x1);
+            hi[u] = __float_as_uint(h0);
+            hi[u + 1] = __float_as_uint(h1);
+            pb[16 * h + u / 2] = pack_bf16x2(x0, x1);
+            plb[16 * h + u / 2] = pack_bf16x2(x0 - h0, x1 - h1);
+          }
+          tmem_st32(tS + 32 * h, hi);
         }
-        tmem_st32(tS + 32 * h, hi);
-        tmem_st32(tS + 64 + 32 * h, lo);
+        tmem_st32(tS + 64, pb);
+        tmem_st32(tS + 96, plb);
       }
       // Lazy correction of O before PV_j: only if some row of this warp moved
       // its reference, and only once PV_{j-1} has landed.
@@ -466,21 +499,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Tensor maps over the split operands: K parts [BH, N, 64] with boxes of
-// 32 floats x 64 keys, V^T parts [BH, 64, Np] with boxes of 32 keys x 64 rows.
-CUresult make_map(CUtensorMap* map, const void* ptr, cuuint64_t inner, cuuint64_t rows, int BH) {
+// 32 floats x 64 keys, V^T parts [BH, 64, Np] with boxes of 128 bytes of keys
+// (32 fp32 or 64 bf16) x 64 rows.
+CUresult make_map(CUtensorMap* map, const void* ptr, cuuint64_t inner, cuuint64_t rows, int BH,
+                  int esize) {
   PFN_encodeTiled enc = get_encode_tiled();
   if (!enc) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[3] = {inner, rows, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {inner * 4, inner * rows * 4};
-  cuuint32_t box[3] = {32, 64, 1};
+  cuuint64_t strides[2] = {inner * esize, inner * rows * esize};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 64, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
+  return enc(map, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             3, const_cast<void*>(ptr), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 struct WsParts {
-  size_t k_bytes, vt_bytes, total;
+  size_t k_bytes, vt_bytes, total;  // vt_bytes: the fp32 V^T_hi part
   int Np;
 };
 
@@ -491,7 +527,7 @@ WsParts ws_parts(int B, int H, int N) {
   w.k_bytes = BH * (size_t)N * kD * 4;
   w.k_bytes = (w.k_bytes + 255) / 256 * 256;
   w.vt_bytes = BH * (size_t)kD * w.Np * 4;
-  w.total = 2 * w.k_bytes + 2 * w.vt_bytes;
+  w.total = 2 * w.k_bytes + 2 * w.vt_bytes;  // V^T_hi, then two bf16 parts of half its size
   return w;
 }
 
@@ -514,8 +550,8 @@ cudaError_t launch_t(const PrefillTf32x3Args& a, const CUtensorMap* maps, float 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], a.q, a.o, a.lse,
-                            BH, a.N, scale_log2, a.err);
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a.q, a.o,
+                            a.lse, BH, a.N, scale_log2, a.err);
 }
 
 }  // namespace
@@ -542,18 +578,21 @@ cudaError_t launch_prefill_tf32x3(const PrefillTf32x3Args& a, cudaStream_t s) {
   float* k_hi = reinterpret_cast<float*>(ws);
   float* k_lo = reinterpret_cast<float*>(ws + w.k_bytes);
   float* vt_hi = reinterpret_cast<float*>(ws + 2 * w.k_bytes);
-  float* vt_lo = reinterpret_cast<float*>(ws + 2 * w.k_bytes + w.vt_bytes);
-  CUtensorMap maps[4];
-  CUresult r = make_map(&maps[0], k_hi, kD, (cuuint64_t)a.N, BH);
-  if (r == CUDA_SUCCESS) r = make_map(&maps[1], k_lo, kD, (cuuint64_t)a.N, BH);
-  if (r == CUDA_SUCCESS) r = make_map(&maps[2], vt_hi, (cuuint64_t)w.Np, kD, BH);
-  if (r == CUDA_SUCCESS) r = make_map(&maps[3], vt_lo, (cuuint64_t)w.Np, kD, BH);
+  __nv_bfloat16* vt_b = reinterpret_cast<__nv_bfloat16*>(ws + 2 * w.k_bytes + w.vt_bytes);
+  __nv_bfloat16* vt_lo_b =
+      reinterpret_cast<__nv_bfloat16*>(ws + 2 * w.k_bytes + w.vt_bytes + w.vt_bytes / 2);
+  CUtensorMap maps[5];
+  CUresult r = make_map(&maps[0], k_hi, kD, (cuuint64_t)a.N, BH, 4);
+  if (r == CUDA_SUCCESS) r = make_map(&maps[1], k_lo, kD, (cuuint64_t)a.N, BH, 4);
+  if (r == CUDA_SUCCESS) r = make_map(&maps[2], vt_hi, (cuuint64_t)w.Np, kD, BH, 4);
+  if (r == CUDA_SUCCESS) r = make_map(&maps[3], vt_b, (cuuint64_t)w.Np, kD, BH, 2);
+  if (r == CUDA_SUCCESS) r = make_map(&maps[4], vt_lo_b, (cuuint64_t)w.Np, kD, BH, 2);
   if (r != CUDA_SUCCESS) {
     attn_set_error("attn_fwd_tf32x3: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return cudaErrorInvalidValue;
   }
   tf32x3_split_kernel<<<dim3((unsigned)(w.Np / 64), (unsigned)(BH < 65535 ? BH : 65535)), 256,
-                        0, s>>>(a.k, a.v, k_hi, k_lo, vt_hi, vt_lo, a.N, w.Np, BH);
+                        0, s>>>(a.k, a.v, k_hi, k_lo, vt_hi, vt_b, vt_lo_b, a.N, w.Np, BH);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
