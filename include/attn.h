@@ -92,9 +92,10 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 /*
  * attn_fwd_tf32x3_workspace_size -- bytes of device workspace that
  * attn_fwd_tf32x3 needs for (B, H, N, D): 2 x B*H*N*64 floats for the split
- * K (each part rounded up to 256 bytes) plus 2 x B*H*64*Np floats for the
- * split, transposed V (Np = N rounded up to a multiple of 64).  Returns 0 for
- * invalid sizes or D != 64.  Pure host arithmetic: no CUDA call.
+ * K (each part rounded up to 256 bytes) plus 2 x B*H*64*Np floats' worth for
+ * the split, transposed V (V_hi in fp32, V and V - V_hi in bf16; Np = N
+ * rounded up to a multiple of 64).  Returns 0 for invalid sizes or D != 64.
+ * Pure host arithmetic: no CUDA call.
  */
 ATTN_API size_t attn_fwd_tf32x3_workspace_size(int B, int H, int N, int D);
 
@@ -104,8 +105,12 @@ ATTN_API size_t attn_fwd_tf32x3_workspace_size(int B, int H, int N, int D);
  * FlashAttention-2 forward of the "FP32 CUDA-core FlashAttention-2 v2" blog,
  * sections 1.2-1.4 and 3.3-3.5, with the tensor cores of its section 5 list
  * of what is left to do).  Every fp32 operand x is split into
- * hi = tf32(x) and lo = tf32(x - hi), and every product is taken as
- * lo*hi + hi*lo + hi*hi on tcgen05 kind::tf32 with fp32 accumulation.
+ * hi = tf32(x) and lo = x - hi.  Q K^T is lo*hi + hi*lo + hi*hi on tcgen05
+ * kind::tf32 (lo rounded to tf32) with fp32 accumulation; in P V the two
+ * cross terms, which carry about 2^-11 of each product, run on bf16 operands
+ * (kind::f16, bf16(P_lo) bf16(V) + bf16(P) bf16(V_lo)) into the same fp32
+ * accumulator as the tf32 hi*hi.  O and LSE stay within 1e-4 of the exact
+ * result on the tested inputs (the fp32 bound).
  *
  *   q, k, v : [B, H, N, 64] float32, contiguous.
  *   o       : [B, H, N, 64] float32 (written).
