@@ -139,3 +139,10 @@ def test_blog_workload_sampled(causal):
     vmin = v.amin(dim=2).numpy()[:, :, None, :]
     vmax = v.amax(dim=2).numpy()[:, :, None, :]
     assert (o >= vmin - TOL_O).all() and (o <= vmax + TOL_O).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_heads_in_a_ragged_last_group(causal):
+    """15 heads: tiles are scheduled in groups of 8 heads, the last group has 7."""
+    q, k, v = mha_inputs(3, 5, 200, 64, torch.float32, seed=26)
+    _check_full(q, k, v, causal, 0.125)
