@@ -133,6 +133,12 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- workloads
 
+# The pages' own figure for exactly this metric and workload, where they print
+# one: the FA2-v2 blog's section 4.1 table (fp32 v2 kernel, RTX 5080).  Other
+# workloads have none, so their vs_baseline stays null.
+PAGE_TFLOPS = {I.FP32_PAGE2.name: 14.45, I.FP32_PAGE2_CAUSAL.name: 12.87}
+
+
 class PrefillLeg:
     kernel = "prefill_bf16_kernel"
 
@@ -587,7 +593,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+        "scaling": "weak",
+        "vs_baseline": (value / PAGE_TFLOPS[main_leg.cfg.name]
+                        if isinstance(main_leg, PrefillLeg) and len(legs) == 1
+                        and main_leg.cfg.name in PAGE_TFLOPS else None),
         "dtype": "bf16" if main_leg.bound in ("tensor", "hbm") else "f32", "data": "synthetic",
         "config": config_of(args.workload, main_leg),
         "wall_ms_per_step": wall_max / args.steps * 1e3,
