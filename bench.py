@@ -153,6 +153,7 @@ class PrefillLeg:
         eb = 2 if cfg.dtype == torch.bfloat16 else 4
         self.bytes = metrics.mha_bytes(cfg.B, cfg.H, cfg.N, cfg.D, eb)
         self.launches_per_call = 1
+        self.host_entry = True  # e2e through attn_fwd_host
         self.bound = "tensor" if cfg.dtype == torch.bfloat16 else "alu"
         self.kernel = "prefill_bf16_kernel" if cfg.dtype == torch.bfloat16 else "prefill_f32_kernel"
         self.src = ("prefill_bf16.cu",) if cfg.dtype == torch.bfloat16 else ("prefill_f32.cu",)
@@ -166,10 +167,28 @@ class PrefillLeg:
         self.hq, self.hk, self.hv = (t.pin_memory() for t in (self.q, self.k, self.v))
         self.ho = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
         self.hl = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        self.hws = None
+        if self.host_entry:
+            c = self.cfg
+            code = (self.pkg.ATTN_DTYPE_F32 if c.dtype == torch.float32
+                    else self.pkg.ATTN_DTYPE_BF16)
+            need = self.pkg.attn_fwd_host_workspace_size(c.B, c.H, c.N, c.D, code)
+            raw = torch.empty(need + 256, dtype=torch.uint8, device=self.dev)
+            off = (-raw.data_ptr()) % 256
+            self.hws = raw[off:off + need]
         self.h2d = sum(t.numel() * t.element_size() for t in (self.hq, self.hk, self.hv))
         self.d2h = self.ho.numel() * self.ho.element_size() + self.hl.numel() * 4
 
     def e2e_run(self):
+        # the host-buffer entry point: copies in, attention, copies out, with
+        # the copies of one chunk of heads overlapping another's attention
+        if self.hws is None:
+            self._e2e_run_copies()
+            return
+        self.pkg.attn_fwd_host(self.hq, self.hk, self.hv, self.ho, self.hl,
+                               causal=self.cfg.causal, scale=self.cfg.scale, workspace=self.hws)
+
+    def _e2e_run_copies(self):
         self.dq.copy_(self.hq, non_blocking=True)
         self.dk.copy_(self.hk, non_blocking=True)
         self.dv.copy_(self.hv, non_blocking=True)
@@ -219,6 +238,7 @@ class Tf32x3Leg(PrefillLeg):
         need = self.pkg.attn_fwd_tf32x3_workspace_size(cfg.B, cfg.H, cfg.N, cfg.D)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         self.bound = "tensor_tf32"
+        self.host_entry = False  # no host-buffer entry: copies around the device call
         self.kernel = "prefill_tf32x3_kernel"
         self.src = ("prefill_tf32x3.cu",)
         self.launches_per_call = 2
@@ -264,15 +284,18 @@ class DecodeLeg:
         self.h2d = sum(t.numel() * t.element_size() for t in
                        (self.hq, self.hkv, self.htable, self.hsl))
         self.d2h = self.ho.numel() * 2 + self.hl.numel() * 4
+        nsm = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        need = self.pkg.mla_decode_host_workspace_size(self.cfg.batch, self.cfg.Hq,
+                                                       self.table.shape[1], self.kv.shape[0], nsm)
+        raw = torch.empty(need + 256, dtype=torch.uint8, device=self.dev)
+        off = (-raw.data_ptr()) % 256
+        self.hws = raw[off:off + need]
 
     def e2e_run(self):
-        self.dq.copy_(self.hq, non_blocking=True)
-        self.dkv.copy_(self.hkv, non_blocking=True)
-        self.dtable.copy_(self.htable, non_blocking=True)
-        self.dsl.copy_(self.hsl, non_blocking=True)
-        self.run()
-        self.ho.copy_(self.o, non_blocking=True)
-        self.hl.copy_(self.lse, non_blocking=True)
+        # the host-buffer entry point: copies in, plan + decode + combine,
+        # copies out, in order on the stream
+        self.pkg.mla_decode_host(self.hq, self.hkv, self.htable, self.hsl, self.ho, self.hl,
+                                 scale=self.cfg.scale, workspace=self.hws)
 
     def value(self, seconds):
         return self.bytes / seconds / 1e9, "GB/s"

@@ -134,6 +134,59 @@ ATTN_API int attn_fwd_tf32x3(const float* q, const float* k, const float* v, flo
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fwd_host_workspace_size -- bytes of device workspace attn_fwd_host
+ * needs: one or two chunk buffers of [q | k | v | o] (ceil(B*H / chunks) heads
+ * of N x D elements each) plus the chunk's LSE, every part rounded up to 256
+ * bytes; chunks = min(B*H, 4).  Returns 0 for a combination attn_fwd does not
+ * build.  Pure host arithmetic: no CUDA call.
+ */
+ATTN_API size_t attn_fwd_host_workspace_size(int B, int H, int N, int D, int dtype);
+
+/*
+ * attn_fwd_host -- attn_fwd on HOST buffers: the same arguments and result,
+ * but q, k, v are read from and o, lse written to host memory (page-locked
+ * memory lets the copies run asynchronously and overlap; pageable memory
+ * works, with copies that block the calling thread).
+ *
+ *   workspace : device buffer, 256-byte aligned, of at least
+ *               attn_fwd_host_workspace_size(...) bytes, owned by the caller
+ *               and not shared with another call in flight.
+ *   stream    : cudaStream_t or NULL; when the stream reaches the end of the
+ *               call's work, o and lse are in host memory.
+ * The B*H heads are cut into up to 4 contiguous chunks.  Chunk c+1 is copied
+ * in and chunk c-1 copied out on two copy streams the library keeps per
+ * device (created on first use), while chunk c runs on `stream`; events order
+ * every hand-over, and the call makes `stream` wait for the last copy out.
+ * Returns after enqueue.  Errors: as attn_fwd, plus WORKSPACE_TOO_SMALL and
+ * MISALIGNED for the workspace, and CUDA for a failed copy or event call.
+ */
+ATTN_API int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int N, int D, int causal, float scale, int dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_host_workspace_size -- bytes of device workspace mla_decode_host
+ * needs for these sizes on a device with num_sms SMs: room for q, the pool,
+ * the table, the lengths, o and lse, then mla_decode's own workspace.
+ * Returns 0 for invalid sizes.  Pure host arithmetic: no CUDA call.
+ */
+ATTN_API size_t mla_decode_host_workspace_size(int B, int Hq, int max_blocks_per_seq,
+                                      int num_blocks, int num_sms);
+
+/*
+ * mla_decode_host -- mla_decode on HOST buffers: q, kv_cache, block_table and
+ * seqlens are copied in from host memory, mla_decode runs, and o, lse are
+ * copied back, all in order on `stream` (any sequence may use any page, so
+ * the pool is copied whole).  workspace: device buffer, 256-byte aligned, of
+ * at least mla_decode_host_workspace_size(...) bytes.  Errors: as
+ * mla_decode, plus MISALIGNED for the workspace and CUDA for a failed copy.
+ */
+ATTN_API int mla_decode_host(const void* q, const void* kv_cache, const int32_t* block_table,
+                    const int32_t* seqlens, void* o, float* lse, int B, int Hq,
+                    float scale, int max_blocks_per_seq, int num_blocks, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode needs.
  *
  *   B, Hq, max_blocks_per_seq : as for mla_decode.

@@ -10,6 +10,10 @@ Entry points (same names as the C ABI):
   attn_fwd_tf32x3(q, k, v, o=None, lse=None, causal=False, scale=None,
                   workspace=None, stream=None)
   attn_fwd_tf32x3_workspace_size(B, H, N, D)
+  attn_fwd_host(q, k, v, o=None, lse=None, causal=False, scale=None,
+                workspace=None, stream=None)          # host tensors in and out
+  mla_decode_host(q, kv_cache, block_table, seqlens, o=None, lse=None,
+                  scale=..., workspace=None, stream=None)
   mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None, scale=...,
              workspace=None, stream=None)
   mla_decode_split(..., pages_per_split=...)
@@ -25,6 +29,8 @@ import os
 
 __all__ = [
     "AttnError", "lib", "attn_fwd", "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size",
+    "attn_fwd_host", "attn_fwd_host_workspace_size", "mla_decode_host",
+    "mla_decode_host_workspace_size",
     "mla_decode", "mla_decode_split",
     "mla_decode_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
     "attn_device_status", "attn_last_error",
@@ -79,6 +85,16 @@ def lib():
         L.attn_fwd_tf32x3.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp,
                                       _sz, _vp]
         L.attn_fwd_tf32x3.restype = _i
+        L.attn_fwd_host_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.attn_fwd_host_workspace_size.restype = _sz
+        L.attn_fwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp,
+                                    _sz, _vp]
+        L.attn_fwd_host.restype = _i
+        L.mla_decode_host_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.mla_decode_host_workspace_size.restype = _sz
+        L.mla_decode_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp,
+                                      _sz, _vp]
+        L.mla_decode_host.restype = _i
         L.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
         L.mla_decode_workspace_size.restype = _sz
         L.mla_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp, _sz,
@@ -197,6 +213,98 @@ def attn_fwd_tf32x3(q, k, v, o=None, lse=None, causal: bool = False,
     _check(lib().attn_fwd_tf32x3(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
                                  int(bool(causal)), scale, _ptr(workspace), workspace.numel(),
                                  _stream_ptr(stream)))
+    return o, lse
+
+
+def _require_host(t, name, dtype, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _device_workspace(workspace, need, device):
+    import torch
+    if workspace is None:
+        # 256 bytes of slack for the alignment the library asks for
+        raw = torch.empty(need + 256, dtype=torch.uint8, device=device)
+        off = (-raw.data_ptr()) % 256
+        workspace = raw[off:off + need]
+    _require(workspace, "workspace", torch.uint8)
+    return workspace
+
+
+def attn_fwd_host_workspace_size(B: int, H: int, N: int, D: int, dtype: int) -> int:
+    return int(lib().attn_fwd_host_workspace_size(B, H, N, D, dtype))
+
+
+def attn_fwd_host(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None,
+                  workspace=None, stream=None):
+    """attn_fwd on HOST tensors (page-locked ones overlap the copies).
+
+    q, k, v: [B,H,N,D] fp32 or bf16 CPU tensors; returns (o, lse) on the host,
+    valid once `stream` has reached the end of the call.
+    """
+    import torch
+    B, H, N, D = q.shape
+    dt = q.dtype
+    code = ATTN_DTYPE_F32 if dt == torch.float32 else ATTN_DTYPE_BF16
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"unsupported dtype {dt}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require_host(t, name, dt, (B, H, N, D))
+    if o is None:
+        o = torch.empty(B, H, N, D, dtype=dt, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, pin_memory=True)
+    _require_host(o, "o", dt, (B, H, N, D))
+    _require_host(lse, "lse", torch.float32, (B, H, N))
+    need = attn_fwd_host_workspace_size(B, H, N, D, code)
+    workspace = _device_workspace(workspace, max(need, 16), torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D,
+                               int(bool(causal)), scale, code, _ptr(workspace),
+                               workspace.numel(), _stream_ptr(stream)))
+    return o, lse
+
+
+def mla_decode_host_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_blocks: int,
+                                   num_sms: int) -> int:
+    return int(lib().mla_decode_host_workspace_size(B, Hq, max_blocks_per_seq, num_blocks,
+                                                    num_sms))
+
+
+def mla_decode_host(q, kv_cache, block_table, seqlens, o=None, lse=None,
+                    scale: float = 1.0 / math.sqrt(192.0), workspace=None, stream=None):
+    """mla_decode on HOST tensors: q [B,128,576] bf16, pool [nb,64,576] bf16,
+    block_table [B,max_blocks] int32, seqlens [B] int32; returns (o, lse) on the host."""
+    import torch
+    B, Hq, _ = q.shape
+    _require_host(q, "q", torch.bfloat16, (B, Hq, MLA_DK))
+    nb = kv_cache.shape[0]
+    _require_host(kv_cache, "kv_cache", torch.bfloat16, (nb, MLA_PAGE, MLA_DK))
+    _require_host(block_table, "block_table", torch.int32)
+    _require_host(seqlens, "seqlens", torch.int32, (B,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks_per_seq]")
+    max_blocks = block_table.shape[1]
+    if o is None:
+        o = torch.empty(B, Hq, MLA_DV, dtype=torch.bfloat16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, pin_memory=True)
+    _require_host(o, "o", torch.bfloat16, (B, Hq, MLA_DV))
+    _require_host(lse, "lse", torch.float32, (B, Hq))
+    dev = torch.cuda.current_device()
+    need = mla_decode_host_workspace_size(B, Hq, max_blocks, nb, _num_sms(dev))
+    workspace = _device_workspace(workspace, max(need, 16), dev)
+    _check(lib().mla_decode_host(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seqlens),
+                                 _ptr(o), _ptr(lse), B, Hq, float(scale), max_blocks, nb,
+                                 _ptr(workspace), workspace.numel(), _stream_ptr(stream)))
     return o, lse
 
 

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_api.cu", "prefill_f32.cu", "prefill_bf16.cu", "prefill_tf32x3.cu",
-           "mla_decode.cu", "mla_absorb.cu"]
+           "mla_decode.cu", "mla_absorb.cu", "host_path.cu"]
 
 
 def nvcc_path() -> str:

@@ -36,7 +36,9 @@ def test_header_declares_the_boundary():
     for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
               "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
               "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out",
-              "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size"]:
+              "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size", "attn_fwd_host",
+              "attn_fwd_host_workspace_size", "mla_decode_host",
+              "mla_decode_host_workspace_size"]:
         assert n in names
 
 
@@ -140,3 +142,33 @@ def test_tf32x3_workspace_and_argument_checks(L):
     need = pkg.attn_fwd_tf32x3_workspace_size(1, 1, 16, 64)
     rc = L.attn_fwd_tf32x3(p, p, p, p, p, 1, 1, 16, 64, 0, 0.1, p, need - 1, None)
     assert rc == pkg.ATTN_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_host_entry_workspace_and_argument_checks(L):
+    """attn_fwd_host / mla_decode_host: workspace arithmetic, host-side rejections."""
+    # 4 chunks of ceil(6/4) = 2 heads: two buffers of [q|k|v|o] + lse
+    per = 2 * 300 * 128 * 2
+    lse = 2 * 300 * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert pkg.attn_fwd_host_workspace_size(2, 3, 300, 128, pkg.ATTN_DTYPE_BF16) == \
+        2 * (4 * r256(per) + r256(lse))
+    # a single head is one chunk: one buffer
+    assert pkg.attn_fwd_host_workspace_size(1, 1, 64, 64, pkg.ATTN_DTYPE_F32) == \
+        4 * r256(64 * 64 * 4) + r256(64 * 4)
+    assert pkg.attn_fwd_host_workspace_size(1, 1, 64, 128, pkg.ATTN_DTYPE_F32) == 0
+    assert pkg.attn_fwd_host_workspace_size(1, 1, 64, 64, 7) == 0
+    assert pkg.mla_decode_host_workspace_size(4, 128, 8, 32, 152) > 32 * 64 * 576 * 2
+    assert pkg.mla_decode_host_workspace_size(4, 64, 8, 32, 152) == 0
+    p = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    assert L.attn_fwd_host(None, p, p, p, p, 1, 1, 16, 64, 0, 0.1, 0, p, 1 << 20, None) == \
+        pkg.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_host(p, p, p, p, p, 1, 1, 16, 96, 0, 0.1, 1, p, 1 << 20, None) == \
+        pkg.ATTN_ERR_UNSUPPORTED
+    assert L.attn_fwd_host(p, p, p, p, p, 1, 1, 16, 64, 0, 0.1, 0, ctypes.c_void_p(272),
+                           1 << 20, None) == pkg.ATTN_ERR_MISALIGNED
+    assert L.attn_fwd_host(p, p, p, p, p, 1, 1, 16, 64, 0, 0.1, 0, p, 16, None) == \
+        pkg.ATTN_ERR_WORKSPACE_TOO_SMALL
+    args = [p] * 6
+    assert L.mla_decode_host(*args, 1, 128, 0.1, 4, 4, None, 0, None) == pkg.ATTN_ERR_INVALID_ARG
+    assert L.mla_decode_host(*args, 1, 64, 0.1, 4, 4, p, 1 << 20, None) == \
+        pkg.ATTN_ERR_UNSUPPORTED
