@@ -128,11 +128,7 @@ inline int max_chunks_for(int B, int max_blocks, int num_sms, int pps) {
   return num_sms / 2;  // per-sequence chunks only when B <= clusters
 }
 
-// Plans with at most this many sequences / chunks search shared-memory copies.
-constexpr int kPlanSmemPrefix = 4096;
-constexpr int kPlanSmemBounds = 1024;
-
-__device__ __forceinline__ int find_range(const int* edges, int n, int x) {
+__device__ __forceinline__ int find_range(const int* __restrict__ edges, int n, int x) {
   // largest i in [0, n) with edges[i] <= x < edges[i+1] (edges non-decreasing)
   int lo = 0, hi = n;
   while (lo < hi) {
@@ -159,13 +155,6 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   __shared__ int warp_sums[32];
   __shared__ int warp_max[32];
   __shared__ int carry, maxn_s, nchunks_s, pps_s, mode_s;
-  // The page prefix and the chunk edges are searched many times (binary
-  // searches of dependent loads); copies in shared memory keep each step at
-  // shared-memory latency.  Larger plans search the global arrays.
-  __shared__ int s_prefix[kPlanSmemPrefix + 1];
-  __shared__ int s_bounds[kPlanSmemBounds + 1];
-  const bool pf_smem = B <= kPlanSmemPrefix;
-  const int* pf = pf_smem ? s_prefix : prefix;
   // launched as a programmatic dependent of whatever precedes it on the
   // stream: wait for it before reading the lengths, then let the decode
   // kernel set itself up while this plan runs
@@ -206,10 +195,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     }
     __syncthreads();
     const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
-    if (b < B) {
-      prefix[b] = incl - n;
-      if (pf_smem) s_prefix[b] = incl - n;
-    }
+    if (b < B) prefix[b] = incl - n;
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) carry = incl;
     __syncthreads();
@@ -219,15 +205,12 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   // chunk length whose chunk count fits the clusters.  Warp 0 finds L with
   // one sequence pair per lane; `cut` counts the chunks of cut sequences.
   __shared__ int len3_s, n3_s, cut3_s;
-  if (threadIdx.x == 0) {
-    prefix[B] = carry;
-    if (pf_smem) s_prefix[B] = carry;
-  }
+  if (threadIdx.x == 0) prefix[B] = carry;
   __syncthreads();
   if (wid == 0) {
     const bool try3 = pps_override <= 0 && 2 * B <= clusters && B <= 64 && carry > 0;
-    const int n0 = (try3 && lane < B) ? pf[lane + 1] - pf[lane] : 0;
-    const int n1 = (try3 && lane + 32 < B) ? pf[lane + 33] - pf[lane + 32] : 0;
+    const int n0 = (try3 && lane < B) ? prefix[lane + 1] - prefix[lane] : 0;
+    const int n1 = (try3 && lane + 32 < B) ? prefix[lane + 33] - prefix[lane + 32] : 0;
     auto warp_sum = [&](int v) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -300,8 +283,6 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
   }
   __syncthreads();
   const int T = carry, mode = mode_s, pps = pps_s, nchunks = nchunks_s;
-  const bool bf_smem = nchunks <= kPlanSmemBounds;
-  const int* bf = bf_smem ? s_bounds : bounds;
   if (mode == 3 && wid == 0) {
     // lane l writes the chunks of sequences l and l + 32, after a scan of
     // the chunk counts gives each sequence its first chunk index
@@ -309,7 +290,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int b = lane + 32 * half;
-      const int n = (b < B) ? pf[b + 1] - pf[b] : 0;
+      const int n = (b < B) ? prefix[b + 1] - prefix[b] : 0;
       const int c = (n + pps - 1) / pps;
       int x = c;
 #pragma unroll
@@ -319,27 +300,22 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
       }
       const int k0 = first + x - c;
       for (int j = 0; j < c; ++j) {
-        const int edge = pf[b] + (int)((long long)j * n / c);
-        bounds[k0 + j] = edge;
-        if (bf_smem) s_bounds[k0 + j] = edge;
+        bounds[k0 + j] = prefix[b] + (int)((long long)j * n / c);
         cstart[k0 + j] = b;
       }
       first += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) {
-      bounds[nchunks] = T;
-      if (bf_smem) s_bounds[nchunks] = T;
-    }
+    if (lane == 0) bounds[nchunks] = T;
   }
   for (int k = threadIdx.x; k <= nchunks && mode != 3; k += blockDim.x) {  // 3: done above
     int x;
     if (mode == 1) {
-      x = pf[k];
+      x = prefix[k];
     } else {
       x = min(k * pps, T);
       if (mode == 2 && k > 0 && k < nchunks) {
-        const int b = find_range(pf, B, x);
-        const int s0 = pf[b], s1 = pf[b + 1];
+        const int b = find_range(prefix, B, x);
+        const int s0 = prefix[b], s1 = prefix[b + 1];
         const int tol = pps / 8;
         if (x - s0 <= s1 - x) {
           if (x - s0 <= tol) x = s0;
@@ -349,10 +325,9 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
       }
     }
     bounds[k] = x;
-    if (bf_smem) s_bounds[k] = x;
     // the sequence holding the chunk's first page (B past the last page):
     // the decode kernel starts each chunk from it without a search
-    if (k < nchunks) cstart[k] = (x < T) ? find_range(pf, B, x) : B;
+    if (k < nchunks) cstart[k] = (x < T) ? find_range(prefix, B, x) : B;
   }
   // The sequences the combine kernel has to finish, in order: empty ones
   // (O = 0, LSE = -inf) and those cut by a chunk edge (partials to merge).
@@ -365,12 +340,12 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     const int b = base + threadIdx.x;
     int f = 0, k0 = -1, k1 = -1;
     if (b < B) {
-      const int pb = pf[b], pe = pf[b + 1];
+      const int pb = prefix[b], pe = prefix[b + 1];
       if (pe == pb) {
         f = 1;
       } else {
-        k0 = find_range(bf, nchunks, pb);
-        k1 = find_range(bf, nchunks, pe - 1);
+        k0 = find_range(bounds, nchunks, pb);
+        k1 = find_range(bounds, nchunks, pe - 1);
         f = k0 != k1;
       }
     }
@@ -396,7 +371,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     if (f) {
       // {sequence, first chunk, last chunk, slot of the first chunk's partial}
       // (a chunk's second segment writes slot 2k + 1); k0 = -1: empty sequence
-      const int first_slot = (k0 >= 0) ? (bf[k0] != pf[b] ? 2 * k0 + 1 : 2 * k0) : -1;
+      const int first_slot = (k0 >= 0) ? (bounds[k0] != prefix[b] ? 2 * k0 + 1 : 2 * k0) : -1;
       clist[incl - 1] = make_int4(b, k0, k1, first_slot);
     }
     __syncthreads();
