@@ -220,12 +220,20 @@ class PrefillLeg:
         while True:
             rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False))
             t0 = time.perf_counter()
-            oracle.mha(self.q, self.k, self.v, c.causal, c.scale, rows=rows, threads=threads)
+            ro, rl = oracle.mha(self.q, self.k, self.v, c.causal, c.scale, rows=rows,
+                                threads=threads)
             dt = time.perf_counter() - t0
             if dt >= budget_s or n >= total_rows:
                 break
             n = int(min(total_rows, n * max(2.0, 1.2 * budget_s / max(dt, 1e-3))))
         desc = f"{len(rows)} random query rows of {total_rows} ({c.name})"
+        self.sample_err = None
+        if getattr(self, "o", None) is not None:
+            # the timed runs' output on the same rows, against the oracle
+            go = self.o.float().cpu().numpy().reshape(-1, c.D)[rows]
+            gl = self.lse.cpu().numpy().reshape(-1)[rows]
+            self.sample_err = {"o": float(np.abs(go - ro).max()),
+                               "lse": float(np.abs(gl - rl).max()), "rows": int(len(rows))}
         return rows_flops(rows) / dt / 1e12, desc, dt
 
 
@@ -313,13 +321,20 @@ class DecodeLeg:
         while True:
             rows = np.sort(rng.choice(total, size=min(n, total), replace=False))
             t0 = time.perf_counter()
-            oracle.mla(self.q, self.kv, self.table, self.sl, c.scale, rows=rows, threads=threads)
+            ro, rl = oracle.mla(self.q, self.kv, self.table, self.sl, c.scale, rows=rows,
+                                threads=threads)
             dt = time.perf_counter() - t0
             if dt >= budget_s or n >= total:
                 break
             n = int(min(total, n * max(2.0, 1.2 * budget_s / max(dt, 1e-3))))
         sample_bytes = self.bytes * (len(rows) / total)
         desc = f"{len(rows)} of {total} (sequence, head) rows ({c.name})"
+        self.sample_err = None
+        if getattr(self, "o", None) is not None and not isinstance(self, LayerLeg):
+            go = self.o.float().cpu().numpy().reshape(-1, 512)[rows]
+            gl = self.lse.cpu().numpy().reshape(-1)[rows]
+            self.sample_err = {"o": float(np.abs(go - ro).max()),
+                               "lse": float(np.abs(gl - rl).max()), "rows": int(len(rows))}
         return sample_bytes / dt / 1e9, desc, dt
 
 
@@ -652,6 +667,16 @@ def main():
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
     roof["peak_source"] = peak_src
+    # the spec denominators beside the measured ones: dense bf16 = SMs x 8192
+    # FLOP/clk x max SM clock (tf32 half of it), HBM 8 TB/s
+    props = torch.cuda.get_device_properties(dev)
+    smax_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    bf16_spec = props.multi_processor_count * 8192 * smax_mhz * 1e6 / 1e12
+    spec = {"tensor": bf16_spec, "tensor_tf32": bf16_spec / 2, "hbm": 8000.0,
+            "alu": roof["peak"]}.get(main_leg.bound)
+    if spec:
+        roof["peak_spec"] = spec
+        roof["frac_spec"] = roof["achieved"] / spec
     sha = source_sha(*main_leg.src)
     roof["traffic"] = committed_traffic(main_leg.kernel, main_leg.workload_name(), sha)
     roof["kernel"] = main_leg.kernel
@@ -682,6 +707,12 @@ def main():
         v, desc, dt = main_leg.oracle_sample(12.0, threads)
         line["cpu_baseline"] = {"value": v, "unit": unit, "cores": threads, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
+        err = getattr(main_leg, "sample_err", None)
+        if err is not None:
+            # the timed GPU output on the sampled rows against the oracle
+            tol = ({"o": 1e-4, "lse": 1e-4} if main_leg.bound in ("alu", "tensor_tf32")
+                   else {"o": 2e-2, "lse": 1e-3})
+            line["cpu_baseline"]["max_abs_err"] = dict(err, tolerance=tol)
     print(json.dumps(line))
 
 
