@@ -32,6 +32,11 @@
  *     nothing was launched and attn_last_error() describes the cause.
  *   - Thread safety: calls may be made from several host threads; the error
  *     message is thread-local.
+ *   - Device addresses of the library's own device variables (the error
+ *     word, the prefill work counters, the fixed decode scratch) are looked
+ *     up once per device and cached for the life of the process.  Do not
+ *     keep using the library after cudaDeviceReset() in the same process:
+ *     the cached addresses belong to the destroyed context.
  */
 #ifndef GB300_ATTN_H_
 #define GB300_ATTN_H_
@@ -80,10 +85,16 @@ extern "C" {
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
  * The bf16 path is one persistent kernel (one CTA per SM) whose CTAs draw
  * Q-tile pairs from a work counter: the call enqueues a 4-byte
- * cudaMemsetAsync of that counter on `stream`, then the kernel.  Counters
- * are a fixed set of 64 per device, used round robin, so at most 64 bf16
+ * cudaMemsetAsync of that counter on `stream`, then the kernel.  Ordinary
+ * calls take one of 64 counters per device in turn, so at most 64 bf16
  * attn_fwd launches may be in flight at once across streams of one device
  * (launches on one stream reuse counters in order and are always safe).
+ * A call made while `stream` is being captured into a CUDA graph gets a
+ * counter of its own that no other call uses (up to 1984 such calls per
+ * device and process; beyond that the call fails with ATTN_ERR_CUDA), so a
+ * replay of the graph may overlap any ordinary launch or any other graph.
+ * Two instantiations of the same captured graph share its counters: do not
+ * run them at the same time.
  */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H, int N, int D, int causal, float scale, int dtype,
@@ -192,12 +203,22 @@ ATTN_API int mla_decode_host(const void* q, const void* kv_cache, const int32_t*
  *   B, Hq, max_blocks_per_seq : as for mla_decode.
  *   num_sms         : SM count of the device that will run the call
  *                     (cudaDevAttrMultiProcessorCount); must be >= 2.
- *   pages_per_split : 0 for the automatic split plan, else the fixed number
- *                     of 64-token pages per split (see mla_decode_split).
  * Returns 0 if an argument is invalid.  Pure host arithmetic: no CUDA call.
  */
 ATTN_API size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_seq,
-                                 int num_sms, int pages_per_split);
+                                 int num_sms);
+
+/*
+ * mla_decode_split_workspace_size -- bytes of device workspace that
+ * mla_decode_split needs: as mla_decode_workspace_size, for a fixed split
+ * length of `pages_per_split` 64-token pages (0 = the automatic plan, the
+ * same size as mla_decode_workspace_size).  A fixed split length can cut the
+ * pages into more chunks than the automatic plan, each with its own partial
+ * results, so the size depends on it.
+ * Returns 0 if an argument is invalid.  Pure host arithmetic: no CUDA call.
+ */
+ATTN_API size_t mla_decode_split_workspace_size(int B, int Hq, int max_blocks_per_seq,
+                                       int num_sms, int pages_per_split);
 
 /*
  * mla_decode -- MLA absorbed decode, one query token per sequence.
@@ -237,7 +258,8 @@ ATTN_API int mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
  * splits of `pages_per_split` 64-token pages along one flat page order
  * (0 = the automatic plan).  The results agree with mla_decode within
  * rounding; it exists to exercise the split/merge path at any split count.
- * The workspace must be sized with the same pages_per_split.
+ * The workspace must be sized by mla_decode_split_workspace_size with the
+ * same pages_per_split.
  */
 ATTN_API int mla_decode_split(const void* q, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seqlens,

@@ -17,7 +17,8 @@ Entry points (same names as the C ABI):
   mla_decode(q, kv_cache, block_table, seqlens, o=None, lse=None, scale=...,
              workspace=None, stream=None)
   mla_decode_split(..., pages_per_split=...)
-  mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms, pages_per_split=0)
+  mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms)
+  mla_decode_split_workspace_size(B, Hq, max_blocks_per_seq, num_sms, pages_per_split=0)
   attn_device_status(stream=None)
   attn_last_error()
 """
@@ -32,7 +33,7 @@ __all__ = [
     "attn_fwd_host", "attn_fwd_host_workspace_size", "mla_decode_host",
     "mla_decode_host_workspace_size",
     "mla_decode", "mla_decode_split",
-    "mla_decode_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
+    "mla_decode_workspace_size", "mla_decode_split_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
     "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
     "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
@@ -95,8 +96,10 @@ def lib():
         L.mla_decode_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp,
                                       _sz, _vp]
         L.mla_decode_host.restype = _i
-        L.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.mla_decode_workspace_size.argtypes = [_i, _i, _i, _i]
         L.mla_decode_workspace_size.restype = _sz
+        L.mla_decode_split_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+        L.mla_decode_split_workspace_size.restype = _sz
         L.mla_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp, _sz,
                                  _vp]
         L.mla_decode.restype = _i
@@ -317,10 +320,14 @@ def attn_fwd_test_skip_load(q, k, v, o, lse, causal: bool, scale: float, skip_lo
                                          _stream_ptr(stream), int(skip_load_index)))
 
 
-def mla_decode_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_sms: int,
-                              pages_per_split: int = 0) -> int:
-    return int(lib().mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms,
-                                               pages_per_split))
+def mla_decode_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_sms: int) -> int:
+    return int(lib().mla_decode_workspace_size(B, Hq, max_blocks_per_seq, num_sms))
+
+
+def mla_decode_split_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_sms: int,
+                                    pages_per_split: int = 0) -> int:
+    return int(lib().mla_decode_split_workspace_size(B, Hq, max_blocks_per_seq, num_sms,
+                                                     pages_per_split))
 
 
 def _num_sms(device) -> int:
@@ -348,7 +355,8 @@ def mla_decode_split(q, kv_cache, block_table, seqlens, o=None, lse=None,
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     _require(o, "o", torch.bfloat16, (B, Hq, MLA_DV))
     _require(lse, "lse", torch.float32, (B, Hq))
-    need = mla_decode_workspace_size(B, Hq, max_blocks, _num_sms(q.device), pages_per_split)
+    need = mla_decode_split_workspace_size(B, Hq, max_blocks, _num_sms(q.device),
+                                           pages_per_split)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _require(workspace, "workspace", torch.uint8)
@@ -370,9 +378,10 @@ def mla_decode_noalloc(q, kv_cache, block_table, seqlens, o=None, lse=None,
                        scale: float = 1.0 / math.sqrt(192.0), stream=None):
     """MLA decode without a workspace: the library's fixed device scratch is used.
 
-    For callers that may not allocate device memory when they call; o and lse
-    must then be passed in.  Calls that can overlap on the GPU share the one
-    scratch array and must be serialised by the caller.
+    For callers that may not allocate device memory when they call, so this
+    wrapper allocates nothing either: o ([B,Hq,512] bf16) and lse ([B,Hq]
+    float32) must be passed in.  Calls that can overlap on the GPU share the
+    one scratch array and must be serialised by the caller.
     """
     import torch
     B, Hq, _ = q.shape
@@ -381,10 +390,8 @@ def mla_decode_noalloc(q, kv_cache, block_table, seqlens, o=None, lse=None,
     _require(kv_cache, "kv_cache", torch.bfloat16, (nb, MLA_PAGE, MLA_DK))
     _require(block_table, "block_table", torch.int32)
     _require(seqlens, "seqlens", torch.int32, (B,))
-    if o is None:
-        o = torch.empty(B, Hq, MLA_DV, dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if o is None or lse is None:
+        raise ValueError("mla_decode_noalloc allocates nothing: pass o and lse")
     _require(o, "o", torch.bfloat16, (B, Hq, MLA_DV))
     _require(lse, "lse", torch.float32, (B, Hq))
     _check(lib().mla_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(block_table),

@@ -198,11 +198,16 @@ extern "C" int attn_fwd_tf32x3(const float* q, const float* k, const float* v, f
 
 // ---------------------------------------------------------------- MLA
 
-extern "C" size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_seq,
-                                            int num_sms, int pages_per_split) {
+extern "C" size_t mla_decode_split_workspace_size(int B, int Hq, int max_blocks_per_seq,
+                                                  int num_sms, int pages_per_split) {
   if (B <= 0 || Hq <= 0 || max_blocks_per_seq <= 0 || num_sms < 2 || pages_per_split < 0)
     return 0;
   return mla_workspace_bytes(B, Hq, max_blocks_per_seq, num_sms, pages_per_split);
+}
+
+extern "C" size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_seq,
+                                            int num_sms) {
+  return mla_decode_split_workspace_size(B, Hq, max_blocks_per_seq, num_sms, 0);
 }
 
 static int mla_impl(const void* q, const void* kv, const int32_t* table, const int32_t* seqlens,

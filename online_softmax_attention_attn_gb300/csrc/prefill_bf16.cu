@@ -713,14 +713,23 @@ long long num_items(int B, int H, int N) {
   return (long long)((n_qt + 1) / 2) * B * H;
 }
 
-// Work-item tickets: each launch takes one counter (round robin over
-// kTicketSlots), zeroes it on its stream, and its CTAs draw items from it.
-// A slot is reused kTicketSlots launches later, by which time a launch on the
-// same stream has finished; launches in flight at once on different streams
-// need distinct slots, so up to kTicketSlots of them may overlap.
-constexpr int kTicketSlots = 64;
+// Work-item tickets: each launch takes one counter, zeroes it on its stream
+// (a 4-byte cudaMemsetAsync before the kernel), and its CTAs draw items from
+// it.  Ordinary launches use kRoundRobinSlots counters in turn: a slot comes
+// back kRoundRobinSlots launches later, by which time a launch on the same
+// stream has finished, so at most kRoundRobinSlots launches on different
+// streams may be in flight at once.  A launch enqueued while its stream is
+// being captured into a CUDA graph gets a slot of its own for good (the
+// graph replays the memset and the kernel on that slot whenever it runs), so
+// a replay never shares a counter with an ordinary launch or another
+// captured one.  The two replays that could still collide are replays of two
+// separate instantiations of one graph running at the same time.
+constexpr int kRoundRobinSlots = 64;
+constexpr int kCapturedSlots = 1984;
+constexpr int kTicketSlots = kRoundRobinSlots + kCapturedSlots;
 __device__ int g_prefill_tickets[kTicketSlots];
 std::atomic<unsigned> g_ticket_next{0};
+int g_captured_next[64] = {};
 void* g_ticket_base[64] = {};
 std::mutex g_ticket_mu;
 
@@ -729,7 +738,11 @@ cudaError_t ticket_for_launch(cudaStream_t s, int** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return e;
   void* basep = nullptr;
+  int idx = 0;
   {
     std::lock_guard<std::mutex> lk(g_ticket_mu);
     if (g_ticket_base[dev] == nullptr) {
@@ -737,8 +750,18 @@ cudaError_t ticket_for_launch(cudaStream_t s, int** out) {
       if (e != cudaSuccess) return e;
     }
     basep = g_ticket_base[dev];
+    if (cap == cudaStreamCaptureStatusActive) {
+      if (g_captured_next[dev] >= kCapturedSlots) {
+        attn_set_error("attn_fwd: more than %d bf16 launches captured into graphs on this device",
+                       kCapturedSlots);
+        return cudaErrorInvalidValue;
+      }
+      idx = kRoundRobinSlots + g_captured_next[dev]++;
+    } else {
+      idx = (int)(g_ticket_next.fetch_add(1) % kRoundRobinSlots);
+    }
   }
-  int* slot = static_cast<int*>(basep) + (g_ticket_next.fetch_add(1) % kTicketSlots);
+  int* slot = static_cast<int*>(basep) + idx;
   e = cudaMemsetAsync(slot, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   *out = slot;

@@ -34,6 +34,7 @@ def L():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
+              "mla_decode_split_workspace_size",
               "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
               "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out",
               "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size", "attn_fwd_host",
@@ -91,8 +92,10 @@ def test_workspace_size_is_host_arithmetic(L):
     assert pkg.mla_decode_workspace_size(0, 128, 64, 152) == 0
     assert pkg.mla_decode_workspace_size(4, 128, 64, 1) == 0
     a = pkg.mla_decode_workspace_size(64, 128, 64, 152)
-    b = pkg.mla_decode_workspace_size(64, 128, 64, 152, pages_per_split=1)
+    b = pkg.mla_decode_split_workspace_size(64, 128, 64, 152, pages_per_split=1)
     assert a > 0 and b >= a
+    assert pkg.mla_decode_split_workspace_size(64, 128, 64, 152, pages_per_split=0) == a
+    assert pkg.mla_decode_split_workspace_size(64, 128, 64, 152, pages_per_split=-1) == 0
 
 
 def test_kernel_info(L):

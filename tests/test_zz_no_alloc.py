@@ -55,6 +55,31 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert np.abs(gl[fin] - ref_l[fin]).max() <= TOL_L
 
 
+def test_noalloc_calls_allocate_no_device_memory():
+    """After a first call (which only looks up the scratch array's address),
+    further calls leave the device's free memory unchanged: nothing is
+    allocated per call, by the library or on its behalf."""
+    L = pkg.lib()
+    dev = torch.device("cuda")
+    lens = [4096, 300, 0, 2000, 64, 1, 3000, 777]
+    q, kv, table, sl = mla_inputs(len(lens), 128, lens, seed=71, paged_random=True)
+    q, kv, table, sl = q.to(dev), kv.to(dev), table.to(dev), sl.to(dev)
+    o = torch.empty(len(lens), 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(len(lens), 128, dtype=torch.float32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (_p(q), _p(kv), _p(table), _p(sl), _p(o), _p(lse), len(lens), 128,
+            ctypes.c_float(1.0 / math.sqrt(192.0)), table.shape[1], kv.shape[0], stream)
+    assert L.mla_decode_noalloc(*args) == pkg.ATTN_OK, pkg.attn_last_error()
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        assert L.mla_decode_noalloc(*args) == pkg.ATTN_OK, pkg.attn_last_error()
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after >= free_before, (free_before, free_after)
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+
+
 def test_noalloc_rejects_batches_beyond_the_fixed_scratch():
     L = pkg.lib()
     dev = torch.device("cuda")
