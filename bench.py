@@ -3,15 +3,29 @@
 A step is one pass of the whole hot path over one batch of synthetic input:
   * bf16 causal MHA prefill, B=4, H=16, N=4096, D=128 (attn_fwd), then
   * bf16 MLA absorbed decode, batch 64, Hq=128, seq 4096 (mla_decode).
-`value` is the prefill's algorithmic TFLOP/s (the first half of the metric);
-the decode's KV-cache GB/s is reported under `decode`.  Kernel times come
-from CUDA events on the launching stream; an L2 flush (a 512 MiB write)
-separates timed steps.  `--workload` selects another single path.
+`value` is the prefill's algorithmic TFLOP/s (the first half of the metric),
+from the median of the per-step CUDA-event times; the decode's KV-cache GB/s
+is reported under `decode`.  Kernel times come from CUDA events on the
+launching stream; an L2 flush (a 512 MiB write) separates timed calls.
+
+The default run also reports
+  * `sustained`: each leg of the step back to back for two seconds, with the
+    SM clock and power sampled inside that window and time x clock;
+  * `configs`: every other workload of the target list (the fp32 small causal
+    case and the fp32 B4 H8 N8192 D64 case, both masks, on the CUDA cores and
+    on the tensor cores; the non-causal bf16 prefill; the paged batch-256
+    decode; the decode batch sweep), each with its median time, throughput,
+    fractions of the measured and spec peaks, and its output checked against
+    the fp64 oracle (every row, or a seeded sample of rows for the largest);
+  * `cpu_baseline`: the oracle's own time on every row of the step's prefill,
+    on the host cores, beside its check of the timed GPU output.
+`--workload` selects one path alone.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload step|prefill|prefill_noncausal|decode|decode_paged|
                               decode_b16|decode_b128|decode_b256|mla_layer|fp32|fp32_causal|
-                              fp32_tc|fp32_tc_causal]
+                              fp32_tc|fp32_tc_causal|fp32_small|fp32_small_tc]
+                  [--no-configs] [--no-sustained] [--no-cpu-baseline]
 
 Multi-GPU: the path shards into independent problems, and every box here has
 one GPU, so N ranks run N independent replicas (weak scaling); value sums
@@ -76,15 +90,18 @@ def committed_traffic(kernel: str, workload: str, sha: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks, power and throttle reasons sampled every 100 ms, with
+    the box's timestamp on every sample, so that each load window (the timed
+    steps, each sustained run) gets the samples taken inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.gpu = gpu_index
+        self.rows = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
@@ -92,17 +109,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
-        self.t_start = self.t_end = None
-
-    def mark_start(self):
-        self.t_start = time.time()
-
-    def mark_end(self):
-        self.t_end = time.time()
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            self.rows = []
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -110,25 +121,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.strip()]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
+        import datetime
+        rows = []
+        for line in out.strip().splitlines():
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax, pw = float(r[2]), float(r[3]), float(r[4])
             except ValueError:
                 continue
-            for name, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
-        # the load lasts most of the sampled window: report the busy half
-        busy = sorted(sm)[len(sm) // 2:] if sm else []
-        return {"sm_mhz": statistics.median(busy) if busy else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            reasons = {n for n, v in zip(self.REASONS, r[6:10]) if v.lower() == "active"}
+            rows.append((ts, sm, smax, pw, reasons))
+        self.rows = rows
+
+    def window(self, windows):
+        """Clock statistics of the samples taken inside any of the (t0, t1) windows."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples_under_load": 0}
+        inside = [r for r in self.rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)]
+        sm = [r[1] for r in inside]
+        reasons = sorted(set().union(*[r[4] for r in inside])) if inside else []
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max((r[2] for r in self.rows), default=None),
+                "power_w_max": max((r[3] for r in inside), default=None),
+                "reasons": reasons, "samples_under_load": len(sm)}
 
 
 # ----------------------------------------------------------------- workloads
@@ -227,14 +246,41 @@ class PrefillLeg:
                 break
             n = int(min(total_rows, n * max(2.0, 1.2 * budget_s / max(dt, 1e-3))))
         desc = f"{len(rows)} random query rows of {total_rows} ({c.name})"
-        self.sample_err = None
-        if getattr(self, "o", None) is not None:
-            # the timed runs' output on the same rows, against the oracle
-            go = self.o.float().cpu().numpy().reshape(-1, c.D)[rows]
-            gl = self.lse.cpu().numpy().reshape(-1)[rows]
-            self.sample_err = {"o": float(np.abs(go - ro).max()),
-                               "lse": float(np.abs(gl - rl).max()), "rows": int(len(rows))}
         return rows_flops(rows) / dt / 1e12, desc, dt
+
+
+    def tolerance(self):
+        return ({"o": 1e-4, "lse": 1e-4} if self.cfg.dtype == torch.float32
+                else {"o": 2e-2, "lse": 1e-3})
+
+    def oracle_check(self, threads: int, max_rows: int):
+        """The last call's output against the fp64 oracle on every query row, or
+        on a seeded random sample of max_rows rows (plus each head's first and
+        last row) when there are more."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        total = c.B * c.H * c.N
+        if total <= max_rows:
+            rows = np.arange(total)
+        else:
+            rng = np.random.default_rng(c.seed)
+            edge = np.concatenate([np.arange(c.B * c.H) * c.N, np.arange(c.B * c.H) * c.N + c.N - 1])
+            rows = np.unique(np.concatenate([rng.choice(total, size=max_rows, replace=False),
+                                             edge]))
+        t0 = time.perf_counter()
+        ro, rl = oracle.mha(self.q, self.k, self.v, c.causal, c.scale,
+                            rows=None if len(rows) == total else rows, threads=threads)
+        dt = time.perf_counter() - t0
+        go = self.o.float().cpu().numpy().reshape(-1, c.D)[rows]
+        gl = self.lse.cpu().numpy().reshape(-1)[rows]
+        i = rows % c.N
+        keys = (i + 1) if c.causal else np.full_like(i, c.N)
+        flops = float((4.0 * c.D * keys).sum())
+        return {"o": float(np.abs(go - ro.reshape(go.shape)).max()),
+                "lse": float(np.abs(gl - rl.reshape(gl.shape)).max()),
+                "rows": int(len(rows)), "of_rows": int(total), "tolerance": self.tolerance(),
+                "oracle_s": dt, "oracle_tflops": flops / dt / 1e12}
 
 
 class Tf32x3Leg(PrefillLeg):
@@ -329,13 +375,42 @@ class DecodeLeg:
             n = int(min(total, n * max(2.0, 1.2 * budget_s / max(dt, 1e-3))))
         sample_bytes = self.bytes * (len(rows) / total)
         desc = f"{len(rows)} of {total} (sequence, head) rows ({c.name})"
-        self.sample_err = None
-        if getattr(self, "o", None) is not None and not isinstance(self, LayerLeg):
-            go = self.o.float().cpu().numpy().reshape(-1, 512)[rows]
-            gl = self.lse.cpu().numpy().reshape(-1)[rows]
-            self.sample_err = {"o": float(np.abs(go - ro).max()),
-                               "lse": float(np.abs(gl - rl).max()), "rows": int(len(rows))}
         return sample_bytes / dt / 1e9, desc, dt
+
+
+    def tolerance(self):
+        return {"o": 2e-2, "lse": 1e-3}
+
+    def oracle_check(self, threads: int, max_rows: int):
+        """The last call's output against the fp64 oracle on every (sequence,
+        head) row, or on a seeded random sample of max_rows rows (plus the
+        first and last rows) when there are more."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        total = c.batch * c.Hq
+        if total <= max_rows:
+            rows = np.arange(total)
+        else:
+            rng = np.random.default_rng(c.seed)
+            rows = np.unique(np.concatenate([rng.choice(total, size=max_rows, replace=False),
+                                             [0, c.Hq - 1, total - 1]]))
+        t0 = time.perf_counter()
+        ro, rl = oracle.mla(self.q, self.kv, self.table, self.sl, c.scale,
+                            rows=None if len(rows) == total else rows, threads=threads)
+        dt = time.perf_counter() - t0
+        ro = ro.reshape(len(rows), 512)
+        rl = rl.reshape(len(rows))
+        go = self.o.float().cpu().numpy().reshape(-1, 512)[rows]
+        gl = self.lse.cpu().numpy().reshape(-1)[rows]
+        fin = np.isfinite(rl)
+        lens = self.sl.numpy()[rows // c.Hq].astype(np.float64)
+        return {"o": float(np.abs(go - ro).max()),
+                "lse": float(np.abs(gl[fin] - rl[fin]).max()) if fin.any() else 0.0,
+                "lse_inf_match": bool(np.array_equal(np.isneginf(gl), np.isneginf(rl))),
+                "rows": int(len(rows)), "of_rows": int(total), "tolerance": self.tolerance(),
+                "oracle_s": dt,
+                "oracle_gbs": float((lens * 1152.0).sum()) / dt / 1e9}
 
 
 class LayerLeg(DecodeLeg):
@@ -400,7 +475,16 @@ class LayerLeg(DecodeLeg):
         return self.bytes * (n / c.batch) / dt / 1e9, desc, dt
 
 
+WORKLOADS = ["prefill", "prefill_noncausal", "decode", "decode_paged", "decode_b16",
+             "decode_b128", "decode_b256", "mla_layer", "fp32", "fp32_causal", "fp32_tc",
+             "fp32_tc_causal", "fp32_small", "fp32_small_tc"]
+
+
 def make_leg(name, dev):
+    if name == "fp32_small":
+        return PrefillLeg(I.FP32_SMALL_CAUSAL, dev)
+    if name == "fp32_small_tc":
+        return Tf32x3Leg(I.FP32_SMALL_CAUSAL, dev)
     if name == "prefill":
         return PrefillLeg(I.BF16_PREFILL, dev)
     if name == "prefill_noncausal":
@@ -507,13 +591,15 @@ def make_leg_cpu(name):
             self.q, self.kv, self.table, self.sl = I.mla_config_inputs(cfg)
             self.bytes = metrics.mla_bytes(self.sl.tolist(), cfg.Hq,
                                            max_blocks=self.table.shape[1])
-    if name in ("prefill", "prefill_noncausal", "fp32", "fp32_causal", "fp32_tc",
-                "fp32_tc_causal"):
-        cfg = {"prefill": I.BF16_PREFILL, "prefill_noncausal": I.BF16_PREFILL_NONCAUSAL,
-               "fp32": I.FP32_PAGE2, "fp32_causal": I.FP32_PAGE2_CAUSAL,
-               "fp32_tc": I.FP32_PAGE2, "fp32_tc_causal": I.FP32_PAGE2_CAUSAL}[name]
-        return _P(cfg)
-    return _D(I.MLA_B64 if name == "decode" else I.MLA_B256_PAGED)
+    mha = {"prefill": I.BF16_PREFILL, "prefill_noncausal": I.BF16_PREFILL_NONCAUSAL,
+           "fp32": I.FP32_PAGE2, "fp32_causal": I.FP32_PAGE2_CAUSAL,
+           "fp32_tc": I.FP32_PAGE2, "fp32_tc_causal": I.FP32_PAGE2_CAUSAL,
+           "fp32_small": I.FP32_SMALL_CAUSAL, "fp32_small_tc": I.FP32_SMALL_CAUSAL}
+    if name in mha:
+        return _P(mha[name])
+    mla = {"decode": I.MLA_B64, "decode_paged": I.MLA_B256_PAGED, "decode_b16": I.MLA_B16,
+           "decode_b128": I.MLA_B128, "decode_b256": I.MLA_B256, "mla_layer": I.MLA_B64}
+    return _D(mla[name])
 
 
 def config_of(workload, leg):
@@ -532,17 +618,97 @@ def config_of(workload, leg):
     return cfg
 
 
+# Every workload of the target list, measured and checked in the default
+# run: (leg name, rows the oracle checks at most: all rows when there are
+# fewer).  The two legs of the step itself are taken from the step's timing.
+CONFIG_LEGS = [
+    ("fp32_small", 1 << 30), ("fp32_small_tc", 1 << 30),
+    ("fp32", 4096), ("fp32_causal", 4096), ("fp32_tc", 4096), ("fp32_tc_causal", 4096),
+    ("prefill", 1 << 30), ("prefill_noncausal", 32768),
+    ("decode", 1 << 30), ("decode_paged", 1 << 30),
+    ("decode_b16", 1 << 30), ("decode_b128", 4096), ("decode_b256", 4096),
+]
+SUSTAINED_S = 2.0
+
+
+def time_calls(leg, reps, flush, stream):
+    """CUDA-event time (ms) of each of `reps` calls, L2 flushed before each."""
+    evs = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        leg.run()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def peak_of(leg, peaks, props, smax_mhz):
+    """(measured peak, spec peak, unit) of the roofline that bounds the leg."""
+    bf16_spec = props.multi_processor_count * 8192 * smax_mhz * 1e6 / 1e12
+    ffma = props.multi_processor_count * 128 * 2 * smax_mhz * 1e6 / 1e12
+    if leg.bound == "tensor":
+        return peaks.get("bf16_tflops"), bf16_spec, "TFLOP/s"
+    if leg.bound == "tensor_tf32":
+        # tf32 dense peak: the measured bf16 peak x the nominal tf32 / bf16
+        # ratio (1.1 / 2.25 PFLOP/s); three MMAs per product cap frac at 1/3
+        return peaks.get("bf16_tflops") * (1.1 / 2.25), bf16_spec / 2, "TFLOP/s"
+    if leg.bound == "hbm":
+        return peaks.get("hbm_gbs"), 8000.0, "GB/s"
+    return ffma, ffma, "TFLOP/s"  # fp32 FFMA on the CUDA cores
+
+
+def achieved_of(leg, ms):
+    if leg.bound == "hbm":
+        return leg.bytes / (ms * 1e-3) / 1e9
+    return leg.flops / (ms * 1e-3) / 1e12
+
+
+def config_entry(leg, times, peaks, props, smax_mhz, check):
+    ms = statistics.median(times)
+    v, unit = leg.value(ms * 1e-3)
+    peak, spec, _ = peak_of(leg, peaks, props, smax_mhz)
+    ach = achieved_of(leg, ms)
+    e = {"workload": leg.workload_name(), "kernel": leg.kernel, "ms": ms,
+         "ms_mean": statistics.fmean(times), "reps": len(times), "value": v, "unit": unit,
+         "frac": ach / peak if peak else None, "frac_spec": ach / spec if spec else None,
+         "bound": leg.bound,
+         "traffic": committed_traffic(leg.kernel, leg.workload_name(), source_sha(*leg.src))}
+    if leg.bound == "tensor_tf32":
+        e["ffma_peak_tflops"] = props.multi_processor_count * 128 * 2 * smax_mhz * 1e6 / 1e12
+    if isinstance(leg, PrefillLeg) and leg.cfg.name in PAGE_TFLOPS:
+        e["page_tflops_rtx5080"] = PAGE_TFLOPS[leg.cfg.name]
+    if check is not None:
+        e["max_abs_err"] = check
+        tol = check["tolerance"]
+        e["parity_ok"] = bool(check["o"] <= tol["o"] and check["lse"] <= tol["lse"]
+                              and check.get("lse_inf_match", True))
+    return e
+
+
+def sustained_run(leg, seconds, flush, stream):
+    """The same call back to back (L2 flushed between calls) for >= `seconds`;
+    returns (per-call ms list, (t0, t1) wall window)."""
+    times = []
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        times += time_calls(leg, 25, flush, stream)
+    return times, (t0, time.time())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="step",
-                    choices=["step", "prefill", "prefill_noncausal", "decode", "decode_paged",
-                             "decode_b16", "decode_b128", "decode_b256", "mla_layer", "fp32",
-                             "fp32_causal", "fp32_tc", "fp32_tc_causal"])
+    ap.add_argument("--workload", default="step", choices=["step"] + WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (the default step measures every one)")
+    ap.add_argument("--no-sustained", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -556,6 +722,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
 
     names = ["prefill", "decode"] if args.workload == "step" else [args.workload]
     legs = []
@@ -566,6 +733,8 @@ def main():
             print(f"# leg {n} unavailable: {e}", file=sys.stderr)
     legs = [lg for lg in legs if _leg_works(lg, pkg)]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3)
 
     # warm-up
     for _ in range(args.warmup):
@@ -574,13 +743,11 @@ def main():
             lg.run()
     pkg.attn_device_status()
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    time.sleep(0.3)
+    # ---- the timed steps: K steps, each leg bracketed by CUDA events
     ev = {id(lg): [] for lg in legs}
     barrier(world)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.mark_start()
+    t_main0 = time.time()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         for lg in legs:
@@ -592,20 +759,26 @@ def main():
             ev[id(lg)].append((a, b))
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    t_main1 = time.time()
     barrier(world)
-    if sampler:
-        sampler.mark_end()
     status = pkg.attn_device_status(raise_on_error=False)
     if status != 0:
         raise SystemExit(f"device error during timing: {pkg.attn_last_error()}")
-    clocks = sampler.stop() if sampler else None
-
-    leg_ms = {id(lg): statistics.fmean(a.elapsed_time(b) for a, b in ev[id(lg)]) for lg in legs}
+    times = {id(lg): [a.elapsed_time(b) for a, b in ev[id(lg)]] for lg in legs}
+    leg_ms = {k: statistics.median(v) for k, v in times.items()}
     step_ms = sum(leg_ms.values())
     step_ms_max = allreduce_max(step_ms, world, dev)
     wall_max = allreduce_max(wall, world, dev)
 
-    # end to end through the public API with pinned host buffers: each leg in
+    # ---- sustained: each leg back to back for a few seconds, its own clocks
+    sus = {}
+    if not args.no_sustained:
+        for lg in legs:
+            sus[id(lg)] = sustained_run(lg, SUSTAINED_S, flush, stream)
+        if pkg.attn_device_status(raise_on_error=False) != 0:
+            raise SystemExit(f"device error in the sustained runs: {pkg.attn_last_error()}")
+
+    # ---- end to end through the public API with pinned host buffers: each leg in
     # its own loop (inputs copied in, the call, outputs read back, a sync)
     e2e_steps = max(3, min(args.steps, 20))
     e2e_s = {}
@@ -623,7 +796,48 @@ def main():
 
     if rank != 0:
         return
+    import oracle
+    threads = oracle.num_threads(0)
     peaks, peak_src = load_peaks()
+    # the timed GPU outputs of the step's legs against the oracle (before the
+    # per-workload table reuses the device)
+    checks = {}
+    if not args.no_cpu_baseline:
+        for lg in legs:
+            checks[id(lg)] = lg.oracle_check(threads, 1 << 30)
+
+    # ---- every other workload of the target list: median of K calls, the
+    # roofline fractions, and the output against the oracle
+    configs = {}
+    if args.workload == "step" and not args.no_configs:
+        main_names = {n: lg for n, lg in zip(names, legs)}
+        for name, max_rows in CONFIG_LEGS:
+            if name in main_names:
+                continue
+            try:
+                lg = make_leg(name, dev)
+            except pkg.AttnError as e:
+                configs[name] = {"unavailable": str(e)}
+                continue
+            if not _leg_works(lg, pkg):
+                configs[name] = {"unavailable": pkg.attn_last_error()}
+                continue
+            for _ in range(3):
+                flush.zero_()
+                lg.run()
+            tt = time_calls(lg, max(args.steps, 20), flush, stream)
+            if pkg.attn_device_status(raise_on_error=False) != 0:
+                raise SystemExit(f"device error in {name}: {pkg.attn_last_error()}")
+            chk = None if args.no_cpu_baseline else lg.oracle_check(threads, max_rows)
+            configs[name] = (lg, tt, chk)
+            del lg
+            torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
+    windows = [(t_main0, t_main1)] + [w for _, w in sus.values()]
+    clocks = sampler.window(windows) if sampler else None
+    smax_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+
     main_leg = legs[0]
     main_ms = leg_ms[id(main_leg)]
     v1, unit = main_leg.value(main_ms * 1e-3)
@@ -637,46 +851,22 @@ def main():
                         and main_leg.cfg.name in PAGE_TFLOPS else None),
         "dtype": "bf16" if main_leg.bound in ("tensor", "hbm") else "f32", "data": "synthetic",
         "config": config_of(args.workload, main_leg),
+        "timing": "median of the per-step CUDA-event times",
+        "median_ms": main_ms,
+        "mean_ms": statistics.fmean(times[id(main_leg)]),
         "wall_ms_per_step": wall_max / args.steps * 1e3,
     }
     # roofline of the dominant kernel
-    if main_leg.bound == "tensor":
-        peak = peaks.get("bf16_tflops")
-        achieved = main_leg.flops / (main_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
-    elif main_leg.bound == "tensor_tf32":
-        # tf32 dense peak: the measured bf16 peak x the nominal tf32 / bf16
-        # ratio (1.1 / 2.25 PFLOP/s); three MMAs per product cap frac at 1/3
-        peak = peaks.get("bf16_tflops") * (1.1 / 2.25)
-        achieved = main_leg.flops / (main_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "peak_dtype": "tf32 (measured bf16 x 1.1/2.25)", "mma_per_product": 3}
-        props = torch.cuda.get_device_properties(dev)
-        smax = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-        roof["ffma_peak"] = props.multi_processor_count * 128 * 2 * smax * 1e6 / 1e12
-    elif main_leg.bound == "hbm":
-        peak = peaks.get("hbm_gbs")
-        achieved = main_leg.bytes / (main_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
-    else:
-        # fp32 FFMA: 152 SMs x 128 lanes x 2 FLOP x max SM clock
-        props = torch.cuda.get_device_properties(dev)
-        smax = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-        peak = props.multi_processor_count * 128 * 2 * smax * 1e6 / 1e12
-        achieved = main_leg.flops / (main_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
-    roof["peak_source"] = peak_src
-    # the spec denominators beside the measured ones: dense bf16 = SMs x 8192
-    # FLOP/clk x max SM clock (tf32 half of it), HBM 8 TB/s
-    props = torch.cuda.get_device_properties(dev)
-    smax_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    bf16_spec = props.multi_processor_count * 8192 * smax_mhz * 1e6 / 1e12
-    spec = {"tensor": bf16_spec, "tensor_tf32": bf16_spec / 2, "hbm": 8000.0,
-            "alu": roof["peak"]}.get(main_leg.bound)
-    if spec:
-        roof["peak_spec"] = spec
-        roof["frac_spec"] = roof["achieved"] / spec
+    peak, spec, runit = peak_of(main_leg, peaks, props, smax_mhz)
+    achieved = achieved_of(main_leg, main_ms)
+    roof = {"bound": "tensor" if main_leg.bound.startswith("tensor") else main_leg.bound,
+            "achieved": achieved, "peak": peak, "unit": runit,
+            "frac": achieved / peak if peak else None, "peak_source": peak_src,
+            "peak_spec": spec, "frac_spec": achieved / spec if spec else None}
+    if main_leg.bound == "tensor_tf32":
+        roof.update(peak_dtype="tf32 (measured bf16 x 1.1/2.25)", mma_per_product=3)
+    if main_leg.bound == "alu":
+        roof["bound"] = "alu"
     sha = source_sha(*main_leg.src)
     roof["traffic"] = committed_traffic(main_leg.kernel, main_leg.workload_name(), sha)
     roof["kernel"] = main_leg.kernel
@@ -693,26 +883,62 @@ def main():
         ms = leg_ms[id(lg)]
         v, u = lg.value(ms * 1e-3)
         ev_, eu_ = lg.value(e2e_s[id(lg)])
+        pk, sp, _ = peak_of(lg, peaks, props, smax_mhz)
         line["decode"] = {"value": v * world, "unit": u, "ms": ms, "workload": lg.workload_name(),
-                          "frac_of_hbm": v / peaks.get("hbm_gbs"),
+                          "frac_of_hbm": v / pk, "frac_of_spec_hbm": v / sp,
+                          "traffic": committed_traffic(lg.kernel, lg.workload_name(),
+                                                       source_sha(*lg.src)),
                           "e2e": {"value": ev_ * world, "unit": eu_,
                                   "h2d_bytes_per_step": lg.h2d, "d2h_bytes_per_step": lg.d2h,
                                   "ms_per_step": e2e_s[id(lg)] * 1e3}}
+
+    # sustained figures with the clocks seen under that load
+    if sus:
+        line["sustained"] = {}
+        for lg in legs:
+            tt, w = sus[id(lg)]
+            ck = sampler.window([w]) if sampler else None
+            ms = statistics.median(tt)
+            v, u = lg.value(ms * 1e-3)
+            pk, sp, _ = peak_of(lg, peaks, props, smax_mhz)
+            ach = achieved_of(lg, ms)
+            entry = {"workload": lg.workload_name(), "seconds": w[1] - w[0], "calls": len(tt),
+                     "median_ms": ms, "value": v, "unit": u, "frac": ach / pk if pk else None,
+                     "frac_spec": ach / sp if sp else None, "clocks": ck}
+            if ck and ck.get("sm_mhz"):
+                # time x clock: millions of SM cycles per call, which stays put
+                # when only the clock moves
+                entry["mcycles_per_call"] = ms * ck["sm_mhz"] / 1e3
+            line["sustained"]["prefill" if isinstance(lg, PrefillLeg) else "decode"] = entry
+
     line["gpu_launches"] = args.steps * sum(_launches(lg, pkg) for lg in legs)
     line["clocks"] = clocks
 
-    if not args.no_cpu_baseline:
-        import oracle
-        threads = oracle.num_threads(0)
-        v, desc, dt = main_leg.oracle_sample(12.0, threads)
-        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": threads, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
-        err = getattr(main_leg, "sample_err", None)
-        if err is not None:
-            # the timed GPU output on the sampled rows against the oracle
-            tol = ({"o": 1e-4, "lse": 1e-4} if main_leg.bound in ("alu", "tensor_tf32")
-                   else {"o": 2e-2, "lse": 1e-3})
-            line["cpu_baseline"]["max_abs_err"] = dict(err, tolerance=tol)
+    # per-workload table: the step's own legs from the timed steps, the rest
+    # measured above
+    if configs or (args.workload == "step" and not args.no_configs):
+        table = {}
+        for name, max_rows in CONFIG_LEGS:
+            if name in names:
+                lg = legs[names.index(name)]
+                table[name] = config_entry(lg, times[id(lg)], peaks, props, smax_mhz,
+                                           checks.get(id(lg)))
+            elif name in configs:
+                c = configs[name]
+                table[name] = c if isinstance(c, dict) else config_entry(
+                    c[0], c[1], peaks, props, smax_mhz, c[2])
+        line["configs"] = table
+
+    if checks:
+        chk = checks[id(main_leg)]
+        rate = (chk["oracle_tflops"] if "oracle_tflops" in chk else chk["oracle_gbs"])
+        line["cpu_baseline"] = {
+            "value": rate, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"all {chk['rows']} query rows of {main_leg.workload_name()}"
+            if chk["rows"] == chk["of_rows"] else
+            f"{chk['rows']} of {chk['of_rows']} rows of {main_leg.workload_name()}",
+            "seconds": chk["oracle_s"],
+            "max_abs_err": {k: chk[k] for k in ("o", "lse", "rows", "tolerance")}}
     print(json.dumps(line))
 
 

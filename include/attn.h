@@ -370,6 +370,48 @@ ATTN_API int attn_fwd_test_skip_load(const void* q, const void* k, const void* v
                             int skip_load_index);
 
 /*
+ * attn_fwd_tf32x3_test_skip_load -- TEST HOOK for the bounded-wait failure
+ * path of attn_fwd_tf32x3.
+ *
+ * Same as attn_fwd_tf32x3, except that the producer warp of every CTA never
+ * issues the loads of K/V block `skip_block` (>= 0, 64 keys per block).  The
+ * S issuer's bounded wait for that block runs out (about 2 s), the kernel
+ * records ATTN_ERR_DEVICE_TIMEOUT, every role of the CTA unwinds (its issued
+ * MMAs complete and its issued copies land before tensor memory is freed)
+ * and attn_device_status() returns the code.  CTAs whose tile visits fewer
+ * blocks finish normally.  Output contents are unspecified.  Not for
+ * production use.
+ */
+ATTN_API int attn_fwd_tf32x3_test_skip_load(const float* q, const float* k, const float* v,
+                                            float* o, float* lse, int B, int H, int N, int D,
+                                            int causal, float scale, void* workspace,
+                                            size_t workspace_bytes, void* stream,
+                                            int skip_block);
+
+/*
+ * mla_decode_test_skip_load -- TEST HOOK for the bounded-wait failure path
+ * of the two-CTA decode cluster.
+ *
+ * Same as mla_decode (automatic plan), except that in every cluster the
+ * producer warp of CTA rank 1 never issues the loads of its pipeline step
+ * `skip_step` (>= 0; one step = one 64-token page of the cluster's work, in
+ * order).  Rank 1's bounded wait for that step runs out (about 2 s); rank 0,
+ * which then never receives rank 1's partial scores for the step, runs out
+ * in its own bounded wait; the kernel records ATTN_ERR_DEVICE_TIMEOUT; both
+ * CTAs unwind, meet at the final cluster barrier (an aborted CTA waits 50 us
+ * first, so that no partial-score store is in flight towards a CTA that has
+ * left) and free their tensor memory.  attn_device_status() returns the code.
+ * Clusters with fewer steps finish normally.  Output contents are
+ * unspecified.  Not for production use.
+ */
+ATTN_API int mla_decode_test_skip_load(const void* q, const void* kv_cache,
+                                       const int32_t* block_table, const int32_t* seqlens,
+                                       void* o, float* lse, int B, int Hq, float scale,
+                                       int max_blocks_per_seq, int num_blocks,
+                                       void* workspace, size_t workspace_bytes,
+                                       void* stream, int skip_step);
+
+/*
  * attn_kv_tiles -- host helper: number of KV tiles of width Bc that the Q
  * tile `q_tile` (rows [q_tile*Br, q_tile*Br + Br)) visits for sequence
  * length N.  Causal: kv_limit = min(q_start + Br, N), else N; the count is

@@ -36,6 +36,7 @@ __all__ = [
     "mla_decode_workspace_size", "mla_decode_split_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
     "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
+    "attn_fwd_tf32x3_test_skip_load", "mla_decode_test_skip_load",
     "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
 ]
 
@@ -81,6 +82,12 @@ def lib():
         L.attn_fwd_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                               _f, _vp, _i]
         L.attn_fwd_test_skip_load.restype = _i
+        L.attn_fwd_tf32x3_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                                     _i, _i, _f, _vp, _sz, _vp, _i]
+        L.attn_fwd_tf32x3_test_skip_load.restype = _i
+        L.mla_decode_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i,
+                                                _i, _vp, _sz, _vp, _i]
+        L.mla_decode_test_skip_load.restype = _i
         L.attn_fwd_tf32x3_workspace_size.argtypes = [_i, _i, _i, _i]
         L.attn_fwd_tf32x3_workspace_size.restype = _sz
         L.attn_fwd_tf32x3.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp,
@@ -318,6 +325,25 @@ def attn_fwd_test_skip_load(q, k, v, o, lse, causal: bool, scale: float, skip_lo
     _check(lib().attn_fwd_test_skip_load(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                          N, D, int(bool(causal)), float(scale),
                                          _stream_ptr(stream), int(skip_load_index)))
+
+
+def attn_fwd_tf32x3_test_skip_load(q, k, v, o, lse, causal: bool, scale: float,
+                                   workspace, skip_block: int, stream=None):
+    """Test hook: attn_fwd_tf32x3 whose producers never load one K/V block."""
+    B, H, N, D = q.shape
+    _check(lib().attn_fwd_tf32x3_test_skip_load(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, int(bool(causal)),
+        float(scale), _ptr(workspace), workspace.numel(), _stream_ptr(stream), int(skip_block)))
+
+
+def mla_decode_test_skip_load(q, kv_cache, block_table, seqlens, o, lse, scale: float,
+                              workspace, skip_step: int, stream=None):
+    """Test hook: mla_decode in which rank 1 of every cluster never loads one step."""
+    B, Hq, _ = q.shape
+    _check(lib().mla_decode_test_skip_load(
+        _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq,
+        float(scale), block_table.shape[1], kv_cache.shape[0], _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream), int(skip_step)))
 
 
 def mla_decode_workspace_size(B: int, Hq: int, max_blocks_per_seq: int, num_sms: int) -> int:

@@ -167,9 +167,9 @@ extern "C" size_t attn_fwd_tf32x3_workspace_size(int B, int H, int N, int D) {
   return prefill_tf32x3_workspace_bytes(B, H, N);
 }
 
-extern "C" int attn_fwd_tf32x3(const float* q, const float* k, const float* v, float* o,
-                               float* lse, int B, int H, int N, int D, int causal, float scale,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+static int tf32x3_impl(const float* q, const float* k, const float* v, float* o, float* lse,
+                       int B, int H, int N, int D, int causal, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream, int debug_skip_block) {
   g_msg[0] = '\0';
   if (!q || !k || !v || !o || !lse || !workspace)
     return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_tf32x3: null pointer argument");
@@ -191,9 +191,28 @@ extern "C" int attn_fwd_tf32x3(const float* q, const float* k, const float* v, f
   int code = ATTN_OK;
   int* err = device_err_word(&code);
   if (!err) return code;
-  PrefillTf32x3Args a{q, k, v, o, lse, B, H, N, D, causal != 0, scale, workspace, err};
+  PrefillTf32x3Args a{q, k, v, o, lse, B, H, N, D, causal != 0, scale, workspace, err,
+                      debug_skip_block};
   return finish_launch(launch_prefill_tf32x3(a, static_cast<cudaStream_t>(stream)),
                        "attn_fwd_tf32x3");
+}
+
+extern "C" int attn_fwd_tf32x3(const float* q, const float* k, const float* v, float* o,
+                               float* lse, int B, int H, int N, int D, int causal, float scale,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return tf32x3_impl(q, k, v, o, lse, B, H, N, D, causal, scale, workspace, workspace_bytes,
+                     stream, -1);
+}
+
+extern "C" int attn_fwd_tf32x3_test_skip_load(const float* q, const float* k, const float* v,
+                                              float* o, float* lse, int B, int H, int N, int D,
+                                              int causal, float scale, void* workspace,
+                                              size_t workspace_bytes, void* stream,
+                                              int skip_block) {
+  if (skip_block < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_tf32x3_test_skip_load: block must be >= 0");
+  return tf32x3_impl(q, k, v, o, lse, B, H, N, D, causal, scale, workspace, workspace_bytes,
+                     stream, skip_block);
 }
 
 // ---------------------------------------------------------------- MLA
@@ -213,7 +232,7 @@ extern "C" size_t mla_decode_workspace_size(int B, int Hq, int max_blocks_per_se
 static int mla_impl(const void* q, const void* kv, const int32_t* table, const int32_t* seqlens,
                     void* o, float* lse, int B, int Hq, float scale, int max_blocks,
                     int num_blocks, void* ws, size_t ws_bytes, int pages_per_split,
-                    void* stream) {
+                    void* stream, int debug_skip_step = -1) {
   g_msg[0] = '\0';
   if (!q || !kv || !table || !seqlens || !o || !lse || !ws)
     return fail(ATTN_ERR_INVALID_ARG, "mla_decode: null pointer argument");
@@ -236,7 +255,7 @@ static int mla_impl(const void* q, const void* kv, const int32_t* table, const i
   int* err = device_err_word(&code);
   if (!err) return code;
   MlaArgs a{q, kv, table, seqlens, o, lse, B, Hq, scale, max_blocks, num_blocks, ws, ws_bytes,
-            pages_per_split, nsm, err};
+            pages_per_split, nsm, err, debug_skip_step};
   return finish_launch(launch_mla_decode(a, static_cast<cudaStream_t>(stream)), "mla_decode");
 }
 
@@ -255,6 +274,18 @@ extern "C" int mla_decode_split(const void* q, const void* kv_cache,
                                 int pages_per_split, void* stream) {
   return mla_impl(q, kv_cache, block_table, seqlens, o, lse, B, Hq, scale, max_blocks_per_seq,
                   num_blocks, workspace, workspace_bytes, pages_per_split, stream);
+}
+
+extern "C" int mla_decode_test_skip_load(const void* q, const void* kv_cache,
+                                         const int32_t* block_table, const int32_t* seqlens,
+                                         void* o, float* lse, int B, int Hq, float scale,
+                                         int max_blocks_per_seq, int num_blocks,
+                                         void* workspace, size_t workspace_bytes,
+                                         void* stream, int skip_step) {
+  if (skip_step < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "mla_decode_test_skip_load: step must be >= 0");
+  return mla_impl(q, kv_cache, block_table, seqlens, o, lse, B, Hq, scale, max_blocks_per_seq,
+                  num_blocks, workspace, workspace_bytes, 0, stream, skip_step);
 }
 
 extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache,

@@ -107,6 +107,7 @@ struct PrefillTf32x3Args {
   float scale;
   void* workspace;  // >= prefill_tf32x3_workspace_bytes(B, H, N)
   int* err;
+  int debug_skip_block;  // test hook: >=0 makes every CTA skip that K/V block's load
 };
 
 struct MlaArgs {
@@ -125,6 +126,7 @@ struct MlaArgs {
   int pages_per_split;
   int num_sms;
   int* err;
+  int debug_skip_step;  // test hook: >=0 makes rank 1 of every cluster skip that step's load
 };
 
 // Each returns a cudaError_t (cudaSuccess on a clean enqueue) and may set a

@@ -430,7 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const int* __restrict__ prefix, const int* __restrict__ bounds,
                       const int* __restrict__ cstart,
                       float* __restrict__ part_lse, float* __restrict__ part_o, int B,
-                      int max_blocks, int num_blocks, float scale_log2, int* err) {
+                      int max_blocks, int num_blocks, float scale_log2, int* err,
+                      int debug_skip_step) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -518,7 +519,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ================= producer: paged K/V (own columns) =================
     if (lane == 0) {
       const uint64_t pol_kv = policy_evict_first();  // every cached row is read once
-      int g = 0, issued = 0;
+      // test hook: rank 1 of every cluster never loads this step
+      const int skip_step = rank == 1 ? debug_skip_step : -1;
+      int g = 0, issued = 0, skipped = -1;
       bool ok = true;
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
@@ -538,6 +541,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = mbar_wait(bar_rope_empty(rslot), (ruse - 1) & 1, abort_flag, err, kSiteKvEmpty,
                              g);
               if (!ok) break;
+            }
+            if (g == skip_step) {
+              skipped = g;
+              issued = g + 1;
+              continue;
             }
             int blk = block_table[(size_t)s.b * max_blocks + t / kPage];
             if (blk < 0 || blk >= num_blocks) {
@@ -561,6 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) {
         const int first = issued > kStages ? issued - kStages : 0;
         for (int gg = first; gg < issued; ++gg) {
+          if (gg == skipped) continue;
           volatile int never = 0;
           mbar_wait(bar_kv_full(gg % kStages), (gg / kStages) & 1, &never, nullptr, kSiteDrain, gg);
         }
@@ -1017,6 +1026,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // After an abort the peer may have left its loops with a partial-score
+  // store to this CTA still in flight, one that this CTA's softmax never
+  // waited for (a store lands in well under a microsecond).  A CTA that
+  // aborted waits 50 us before it arrives at the cluster barrier below, so
+  // the peer cannot leave while one of this CTA's own stores is in flight.
+  if (*abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {
+    }
+  }
   cluster_sync();  // no CTA leaves while its peer may still touch its smem
   if (warp == 5) {
     tc_fence_after();
@@ -1219,7 +1238,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
                          static_cast<__nv_bfloat16*>(a.o), a.lse, (const int*)hdr,
                          (const int*)prefix, (const int*)bounds, (const int*)cstart, plse, po,
                          a.B, a.max_blocks,
-                         a.num_blocks, scale_log2, a.err);
+                         a.num_blocks, scale_log2, a.err, a.debug_skip_step);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(4 * a.num_sms, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);

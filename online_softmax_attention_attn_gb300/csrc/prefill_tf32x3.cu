@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tmVb,
                           const __grid_constant__ CUtensorMap tmVlb,
                           const float* __restrict__ q, float* __restrict__ o,
-                          float* __restrict__ lse, int BH, int N, float scale_log2, int* err) {
+                          float* __restrict__ lse, int BH, int N, float scale_log2, int* err,
+                          int debug_skip_block) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: swizzle atoms must start on a 1024-byte boundary.
   const uint32_t raw = smem_u32(smem_raw);
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, j);
           if (!ok) break;
         }
+        if (j == debug_skip_block) continue;  // test hook: this block never arrives
         const uint32_t dst = sRing + s * kStageBytes;
         const uint32_t bar = bar_kv_full(s);
         mbar_arrive_expect_tx(bar, kStageBytes);
@@ -270,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let every copy this thread started land before the CTA unwinds
         const int first = j > kStages ? j - kStages : 0;
         for (int x = first; x < j; ++x) {
+          if (x == debug_skip_block) continue;
           volatile int never = 0;
           mbar_wait(bar_kv_full(x % kStages), (x / kStages) & 1, &never, nullptr, kSiteDrain,
                     x);
@@ -556,7 +559,7 @@ cudaError_t launch_t(const PrefillTf32x3Args& a, const CUtensorMap* maps, float 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a.q, a.o,
-                            a.lse, BH, a.N, scale_log2, a.err);
+                            a.lse, BH, a.N, scale_log2, a.err, a.debug_skip_block);
 }
 
 }  // namespace

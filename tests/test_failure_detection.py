@@ -51,3 +51,79 @@ def test_skip_hook_rejects_bad_index():
     with pytest.raises(pkg.AttnError):
         pkg.attn_fwd_test_skip_load(q, q, q, q.clone(), torch.empty(1, 1, 128, device=dev),
                                     False, 0.1, 0)
+
+
+def test_stuck_tf32x3_pipeline_reports_timeout_and_context_survives():
+    """attn_fwd_tf32x3 with block 1 never loaded: the S issuer's bounded wait
+    runs out in every CTA, the CTAs unwind, and the next call is correct."""
+    dev = torch.device("cuda")
+    q, k, v = mha_inputs(1, 1, 512, 64, torch.float32, seed=81)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(dq)
+    lse = torch.empty(1, 1, 512, dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.attn_fwd_tf32x3_workspace_size(1, 1, 512, 64), dtype=torch.uint8,
+                     device=dev)
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    t0 = time.time()
+    pkg.attn_fwd_tf32x3_test_skip_load(dq, dk, dv, o, lse, True, 0.125, ws, 1)
+    code = pkg.attn_device_status(raise_on_error=False)
+    elapsed = time.time() - t0
+    assert code == pkg.ATTN_ERR_DEVICE_TIMEOUT, pkg.attn_last_error()
+    assert "wait ran out" in pkg.attn_last_error()
+    assert elapsed < 30
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    o2, lse2 = pkg.attn_fwd_tf32x3(dq, dk, dv, causal=True, scale=0.125, workspace=ws)
+    pkg.attn_device_status()
+    ro, rl = oracle.mha(q, k, v, True, 0.125)
+    assert np.abs(o2.cpu().numpy() - ro).max() <= 1e-4
+    assert np.abs(lse2.cpu().numpy() - rl).max() <= 1e-4
+
+
+def test_stuck_decode_cluster_reports_timeout_and_context_survives():
+    """mla_decode in which rank 1 of every cluster never loads its fourth
+    step: rank 1 times out waiting for the page, rank 0 times out waiting for
+    rank 1's partial scores, both CTAs of every pair meet at the final cluster
+    barrier and free their tensor memory, and the next call is correct."""
+    from online_softmax_attention_attn_gb300.inputs import mla_inputs
+    dev = torch.device("cuda")
+    lens = [512] * 64  # one chunk of 8 pages per sequence
+    scale = 1.0 / math.sqrt(192.0)
+    q, kv, table, sl = mla_inputs(len(lens), 128, lens, seed=82, paged_random=True)
+    dq, dkv, dt, dsl = q.to(dev), kv.to(dev), table.to(dev), sl.to(dev)
+    o = torch.empty(len(lens), 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(len(lens), 128, dtype=torch.float32, device=dev)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    ws = torch.empty(pkg.mla_decode_workspace_size(len(lens), 128, table.shape[1], nsm),
+                     dtype=torch.uint8, device=dev)
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    t0 = time.time()
+    pkg.mla_decode_test_skip_load(dq, dkv, dt, dsl, o, lse, scale, ws, 3)
+    code = pkg.attn_device_status(raise_on_error=False)
+    elapsed = time.time() - t0
+    assert code == pkg.ATTN_ERR_DEVICE_TIMEOUT, pkg.attn_last_error()
+    assert "wait ran out" in pkg.attn_last_error()
+    assert elapsed < 30
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    o2, lse2 = pkg.mla_decode(dq, dkv, dt, dsl, scale=scale, workspace=ws)
+    pkg.attn_device_status()
+    ro, rl = oracle.mla(q, kv, table, sl, scale)
+    assert np.abs(o2.float().cpu().numpy() - ro).max() <= 2e-2
+    assert np.abs(lse2.cpu().numpy() - rl).max() <= 1e-3
+
+
+def test_decode_and_tf32x3_skip_hooks_reject_bad_index():
+    dev = torch.device("cuda")
+    z = torch.zeros(1, 1, 128, 64, dtype=torch.float32, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    with pytest.raises(pkg.AttnError):
+        pkg.attn_fwd_tf32x3_test_skip_load(z, z, z, z.clone(),
+                                           torch.empty(1, 1, 128, device=dev), False, 0.1, ws,
+                                           -1)
+    qm = torch.zeros(1, 128, 576, dtype=torch.bfloat16, device=dev)
+    kv = torch.zeros(1, 64, 576, dtype=torch.bfloat16, device=dev)
+    table = torch.zeros(1, 1, dtype=torch.int32, device=dev)
+    sl = torch.full((1,), 64, dtype=torch.int32, device=dev)
+    with pytest.raises(pkg.AttnError):
+        pkg.mla_decode_test_skip_load(qm, kv, table, sl,
+                                      torch.empty(1, 128, 512, dtype=torch.bfloat16, device=dev),
+                                      torch.empty(1, 128, device=dev), 0.1, ws, -1)

@@ -165,12 +165,22 @@ def test_scores_jump_on_a_later_page():
     _check(q, kv, table, sl, o, lse)
 
 
-def test_decode_batch64_workload_sampled():
-    _sampled(MLA_B64, 192, 1)
+def _all_rows(cfg):
+    q, kv, table, sl = mla_config_inputs(cfg)
+    o, lse = _gpu(q, kv, table, sl)
+    _check(q, kv, table, sl, o, lse)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
 
 
-def test_decode_batch256_paged_workload_sampled():
-    _sampled(MLA_B256_PAGED, 192, 2)
+def test_decode_batch64_workload_every_row():
+    """Every (sequence, head) row of the batch-64, seq-4096 workload."""
+    _all_rows(MLA_B64)
+
+
+def test_decode_batch256_paged_workload_every_row():
+    """Every row of the batch-256 paged workload (ragged lengths 1024-4096,
+    random page permutation, split-KV partials merged by the combine)."""
+    _all_rows(MLA_B256_PAGED)
 
 
 @pytest.mark.parametrize("cfg", [MLA_B16, MLA_B128, MLA_B256], ids=lambda c: str(c.batch))
