@@ -73,7 +73,7 @@ constexpr int kVlbOff = kVbOff + kAtomBytes;  // bf16(V_lo)^T
 constexpr int kStageBytes = kVlbOff + kAtomBytes;  // K_hi, K_lo, V^T_hi, two bf16 V^T
 constexpr int kStages = 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kHeadGroup = 8;              // heads whose tiles are scheduled together
+constexpr int kHeadGroup = 4;              // heads whose tiles are scheduled together
 
 constexpr int kRingOff = 0;
 constexpr int kBarOff = kRingOff + kStages * kStageBytes;
@@ -195,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Blocks run in launch order, in groups of kHeadGroup heads: the CTAs in
-  // flight share one group's split K/V in L2 (8 MB per head at N = 8192).
+  // flight share one group's split K/V in L2 (8 MB per head at N = 8192, so
+  // 32 MB per group; groups of 8 heads let part of it be evicted before its
+  // last reader and read K/V from DRAM again).
   // Within a group the heaviest causal tiles come first, across its heads.
   const int n_qt = (N + kBM - 1) / kBM;
   const int group = (int)(blockIdx.x / (unsigned)(kHeadGroup * n_qt));
