@@ -303,13 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_t = Q_t K_j^T (its wait also covers V_j, which shares the stage).
       // The tile is a compile-time constant so that the issue path carries
       // no per-tile selects: every instruction of this thread delays the pipe.
-      auto issue_s = [&](auto tile, int j) -> bool {
+      // Where the other tile's S of the same block was issued just before
+      // (the steady part), the stage is known to be full and the wait is
+      // left out.
+      using Wait = std::true_type;
+      using NoWait = std::false_type;
+      auto issue_s = [&](auto tile, int j, auto wait) -> bool {
         constexpr int t = decltype(tile)::value;
         const int x = kv + j;
         const int slot = x % C::kStages;
-        if (!mbar_wait(bar_kv_full(slot), (x / C::kStages) & 1, abort_flag, err, kSiteKvFull, j))
-          return false;
-        tc_fence_after();
+        if constexpr (decltype(wait)::value) {
+          if (!mbar_wait(bar_kv_full(slot), (x / C::kStages) & 1, abort_flag, err, kSiteKvFull,
+                         j))
+            return false;
+          tc_fence_after();
+        }
         const uint64_t qb = qd0 + (uint64_t)(t * (C::kTileBytes >> 4));
         const uint64_t kb = kd0 + (uint64_t)(slot * (C::kStageBytes >> 4));
         const uint32_t dS = tbase + C::kColS + t * 128;
@@ -380,13 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(bar_q_full(0), qn0 & 1, abort_flag, err, kSiteQFull, k);
         if (ok) {
           tc_fence_after();
-          ok = issue_s(Tile0{}, 0);
+          ok = issue_s(Tile0{}, 0, Wait{});
         }
         if (ok && T1 > 0) {
           ok = mbar_wait(bar_q_full(1), qn1 & 1, abort_flag, err, kSiteQFull, k);
           if (ok) {
             tc_fence_after();
-            ok = issue_s(Tile1{}, 0);
+            ok = issue_s(Tile1{}, 0, Wait{});
           }
         }
         // q_free[t] is committed right after the tile's last S: the producer
@@ -395,12 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && T1 == 1) tc_commit(bar_q_free(1));
         if (ok) ok = wait_o_free(Tile0{}) && issue_pv(Tile0{}, 0);
         if (ok && T0 > 1) {
-          ok = issue_s(Tile0{}, 1);
+          ok = issue_s(Tile0{}, 1, Wait{});
           if (ok && T0 == 2) tc_commit(bar_q_free(0));
         }
         if (ok && T1 > 0) ok = wait_o_free(Tile1{}) && issue_pv(Tile1{}, 0);
         if (ok && T1 > 1) {
-          ok = issue_s(Tile1{}, 1);
+          ok = issue_s(Tile1{}, 1, Wait{});
           if (ok && T1 == 2) tc_commit(bar_q_free(1));
         }
         // blocks 1.. : the steady part has no last S of either tile and so
@@ -411,23 +419,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (T1 > 0) {
           for (; j < j_tail && ok; ++j) {
             ok = issue_pv(Tile0{}, j);
-            if (ok) ok = issue_s(Tile0{}, j + 1);
+            if (ok) ok = issue_s(Tile0{}, j + 1, Wait{});
             if (ok) ok = issue_pv(Tile1{}, j);
-            if (ok) ok = issue_s(Tile1{}, j + 1);
+            if (ok) ok = issue_s(Tile1{}, j + 1, NoWait{});
           }
         }
         for (; j < Tmax && ok; ++j) {
           if (j < T0) {
             ok = issue_pv(Tile0{}, j);
             if (ok && j + 1 < T0) {
-              ok = issue_s(Tile0{}, j + 1);
+              ok = issue_s(Tile0{}, j + 1, Wait{});
               if (ok && j + 2 == T0) tc_commit(bar_q_free(0));
             }
           }
           if (ok && j < T1) {
             ok = issue_pv(Tile1{}, j);
             if (ok && j + 1 < T1) {
-              ok = issue_s(Tile1{}, j + 1);
+              ok = issue_s(Tile1{}, j + 1, Wait{});
               if (ok && j + 2 == T1) tc_commit(bar_q_free(1));
             }
           }
