@@ -6,7 +6,8 @@ synchronise the device at a bad time), so they cannot pass mla_decode a
 workspace.  mla_decode_noalloc runs the same kernels with the plan and split
 partials in a fixed device array inside the library.  This test calls it
 through the C ABI, twice in a row, and checks it against mla_decode (which
-uses a caller workspace) within the decode tolerance.  It sits in its own
+uses a caller workspace) and against the fp64 oracle, within the decode
+tolerance.  It sits in its own
 file, collected last, and passes alone in a fresh process or after the rest
 of the suite.
 """
@@ -17,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import online_softmax_attention_attn_gb300 as pkg
 from online_softmax_attention_attn_gb300.inputs import mla_inputs
 
@@ -39,6 +41,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
     ref_o, ref_l = pkg.mla_decode(q, kv, table, sl, scale=scale)
     pkg.attn_device_status()
     ref_o, ref_l = ref_o.float().cpu().numpy(), ref_l.cpu().numpy()
+    oro, orl = oracle.mla(q.cpu(), kv.cpu(), table.cpu(), sl.cpu(), scale)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for _ in range(2):
         o = torch.full((len(lens), 128, 512), float("nan"), dtype=torch.bfloat16, device=dev)
@@ -53,6 +56,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
         fin = np.isfinite(ref_l)
         assert np.array_equal(np.isneginf(gl), np.isneginf(ref_l))
         assert np.abs(gl[fin] - ref_l[fin]).max() <= TOL_L
+        # and against the fp64 oracle itself
+        assert np.abs(go - oro).max() <= TOL_O
+        assert np.array_equal(np.isneginf(gl), np.isneginf(orl))
+        ofin = np.isfinite(orl)
+        assert np.abs(gl[ofin] - orl[ofin]).max() <= TOL_L
 
 
 def test_noalloc_calls_allocate_no_device_memory():
