@@ -140,42 +140,30 @@ __device__ __forceinline__ int find_range(const int* __restrict__ edges, int n, 
 }
 
 // ---- plan -------------------------------------------------------------------
-// One CTA of 256 threads (small enough to share an SM with a decode CTA, so
-// no decode cluster waits for the plan's SM).  Validates lengths, writes the
-// exclusive page prefix, then the chunk edges, by a time model: per-sequence
-// chunks (no partials); with fewer sequences than clusters, each sequence cut
-// into near-equal chunks of its own; else ceil(T / clusters) pages per chunk
-// with each cut moved to a sequence start within 1/8 chunk; or a fixed split
-// length when one is forced.  The prefix and the chunk edges are kept in
-// shared memory when they fit, so the only global read on the way is the
-// lengths themselves; every result is also written to the workspace.
-constexpr int kPlanThreads = 256;
-constexpr int kPlanSmemB = 1024;       // sequences whose prefix stays in shared memory
-constexpr int kPlanSmemChunks = 256;   // chunk edges kept in shared memory
-
-// (at most 40 registers a thread, so that the plan CTA and a decode CTA fit
-// in one SM's register file together)
-__global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
-    const int32_t* __restrict__ seqlens, int B, int max_blocks, int clusters, int pps_override,
-    int* __restrict__ hdr, int* __restrict__ prefix, int* __restrict__ bounds,
-    int* __restrict__ cstart, int4* __restrict__ clist, int* err) {
+// One CTA.  Validates lengths, writes the exclusive page prefix, then the
+// chunk edges, by a time model: per-sequence chunks (no partials); with fewer
+// sequences than clusters, each sequence cut into near-equal chunks of its
+// own; else ceil(T / clusters) pages per chunk with each cut moved to a
+// sequence start within 1/8 chunk; or a fixed split length when one is forced.
+__global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restrict__ seqlens,
+                                                        int B, int max_blocks, int clusters,
+                                                        int pps_override, int* __restrict__ hdr,
+                                                        int* __restrict__ prefix,
+                                                        int* __restrict__ bounds,
+                                                        int* __restrict__ cstart,
+                                                        int4* __restrict__ clist, int* err) {
   __shared__ int warp_sums[32];
   __shared__ int warp_max[32];
   __shared__ int carry, maxn_s, nchunks_s, pps_s, mode_s;
-  __shared__ int s_prefix[kPlanSmemB + 1];
-  __shared__ int s_bounds[kPlanSmemChunks + 1];
   // launched as a programmatic dependent of whatever precedes it on the
   // stream: wait for it before reading the lengths, then let the decode
   // kernel set itself up while this plan runs
   grid_dependency_wait();
   grid_launch_dependents();
-  const bool small = B <= kPlanSmemB;
-  int* pf = small ? s_prefix : prefix;  // where this kernel reads the prefix back
   if (threadIdx.x == 0) { carry = 0; maxn_s = 0; }
   __syncthreads();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nwarps = kPlanThreads / 32;
-  for (int base = 0; base < B; base += kPlanThreads) {
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int n = 0;
     if (b < B) {
@@ -194,8 +182,8 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
     if (lane == 0) warp_max[wid] = mx;
     __syncthreads();
     if (wid == 0) {
-      int w = lane < nwarps ? warp_sums[lane] : 0;
-      int m = lane < nwarps ? warp_max[lane] : 0;
+      int w = warp_sums[lane];
+      int m = warp_max[lane];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, w, off);
@@ -207,12 +195,9 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
     }
     __syncthreads();
     const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
-    if (b < B) {
-      prefix[b] = incl - n;
-      if (small) s_prefix[b] = incl - n;
-    }
+    if (b < B) prefix[b] = incl - n;
     __syncthreads();
-    if (threadIdx.x == kPlanThreads - 1) carry = incl;
+    if (threadIdx.x == blockDim.x - 1) carry = incl;
     __syncthreads();
   }
   // Fewer than half as many sequences as clusters (at most 64): each sequence
@@ -220,15 +205,12 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
   // chunk length whose chunk count fits the clusters.  Warp 0 finds L with
   // one sequence pair per lane; `cut` counts the chunks of cut sequences.
   __shared__ int len3_s, n3_s, cut3_s;
-  if (threadIdx.x == 0) {
-    prefix[B] = carry;
-    if (small) s_prefix[B] = carry;
-  }
+  if (threadIdx.x == 0) prefix[B] = carry;
   __syncthreads();
   if (wid == 0) {
     const bool try3 = pps_override <= 0 && 2 * B <= clusters && B <= 64 && carry > 0;
-    const int n0 = (try3 && lane < B) ? pf[lane + 1] - pf[lane] : 0;
-    const int n1 = (try3 && lane + 32 < B) ? pf[lane + 33] - pf[lane + 32] : 0;
+    const int n0 = (try3 && lane < B) ? prefix[lane + 1] - prefix[lane] : 0;
+    const int n1 = (try3 && lane + 32 < B) ? prefix[lane + 33] - prefix[lane + 32] : 0;
     auto warp_sum = [&](int v) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -301,8 +283,6 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
   }
   __syncthreads();
   const int T = carry, mode = mode_s, pps = pps_s, nchunks = nchunks_s;
-  const bool small_b = nchunks <= kPlanSmemChunks;
-  int* pb = small_b ? s_bounds : bounds;  // where this kernel reads the edges back
   if (mode == 3 && wid == 0) {
     // lane l writes the chunks of sequences l and l + 32, after a scan of
     // the chunk counts gives each sequence its first chunk index
@@ -310,7 +290,7 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int b = lane + 32 * half;
-      const int n = (b < B) ? pf[b + 1] - pf[b] : 0;
+      const int n = (b < B) ? prefix[b + 1] - prefix[b] : 0;
       const int c = (n + pps - 1) / pps;
       int x = c;
 #pragma unroll
@@ -320,27 +300,22 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
       }
       const int k0 = first + x - c;
       for (int j = 0; j < c; ++j) {
-        const int e = pf[b] + (int)((long long)j * n / c);
-        bounds[k0 + j] = e;
-        if (small_b) s_bounds[k0 + j] = e;
+        bounds[k0 + j] = prefix[b] + (int)((long long)j * n / c);
         cstart[k0 + j] = b;
       }
       first += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) {
-      bounds[nchunks] = T;
-      if (small_b) s_bounds[nchunks] = T;
-    }
+    if (lane == 0) bounds[nchunks] = T;
   }
-  for (int k = threadIdx.x; k <= nchunks && mode != 3; k += kPlanThreads) {  // 3: done above
+  for (int k = threadIdx.x; k <= nchunks && mode != 3; k += blockDim.x) {  // 3: done above
     int x;
     if (mode == 1) {
-      x = pf[k];
+      x = prefix[k];
     } else {
       x = min(k * pps, T);
       if (mode == 2 && k > 0 && k < nchunks) {
-        const int b = find_range(pf, B, x);
-        const int s0 = pf[b], s1 = pf[b + 1];
+        const int b = find_range(prefix, B, x);
+        const int s0 = prefix[b], s1 = prefix[b + 1];
         const int tol = pps / 8;
         if (x - s0 <= s1 - x) {
           if (x - s0 <= tol) x = s0;
@@ -350,10 +325,9 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
       }
     }
     bounds[k] = x;
-    if (small_b) s_bounds[k] = x;
     // the sequence holding the chunk's first page (B past the last page):
     // the decode kernel starts each chunk from it without a search
-    if (k < nchunks) cstart[k] = (mode == 1) ? k : ((x < T) ? find_range(pf, B, x) : B);
+    if (k < nchunks) cstart[k] = (x < T) ? find_range(prefix, B, x) : B;
   }
   // The sequences the combine kernel has to finish, in order: empty ones
   // (O = 0, LSE = -inf) and those cut by a chunk edge (partials to merge).
@@ -362,18 +336,16 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
   __shared__ int ccarry;
   if (threadIdx.x == 0) ccarry = 0;
   __syncthreads();
-  for (int base = 0; base < B; base += kPlanThreads) {
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int f = 0, k0 = -1, k1 = -1;
     if (b < B) {
-      const int p0 = pf[b], p1 = pf[b + 1];
-      if (p1 == p0) {
+      const int pb = prefix[b], pe = prefix[b + 1];
+      if (pe == pb) {
         f = 1;
-      } else if (mode == 1) {
-        k0 = k1 = b;  // chunk b is sequence b, whole
       } else {
-        k0 = find_range(pb, nchunks, p0);
-        k1 = find_range(pb, nchunks, p1 - 1);
+        k0 = find_range(bounds, nchunks, pb);
+        k1 = find_range(bounds, nchunks, pe - 1);
         f = k0 != k1;
       }
     }
@@ -386,7 +358,7 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
     if (lane == 31) warp_sums[wid] = x;
     __syncthreads();
     if (wid == 0) {
-      int w = lane < nwarps ? warp_sums[lane] : 0;
+      int w = warp_sums[lane];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, w, off);
@@ -399,11 +371,11 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
     if (f) {
       // {sequence, first chunk, last chunk, slot of the first chunk's partial}
       // (a chunk's second segment writes slot 2k + 1); k0 = -1: empty sequence
-      const int first_slot = (k0 >= 0) ? (pb[k0] != pf[b] ? 2 * k0 + 1 : 2 * k0) : -1;
+      const int first_slot = (k0 >= 0) ? (bounds[k0] != prefix[b] ? 2 * k0 + 1 : 2 * k0) : -1;
       clist[incl - 1] = make_int4(b, k0, k1, first_slot);
     }
     __syncthreads();
-    if (threadIdx.x == kPlanThreads - 1) ccarry = incl;
+    if (threadIdx.x == blockDim.x - 1) ccarry = incl;
     __syncthreads();
   }
   if (threadIdx.x == 0) hdr[4] = ccarry;
@@ -413,31 +385,14 @@ __global__ void __launch_bounds__(kPlanThreads, 6) mla_plan_kernel(
 struct Seg {
   int b, p0, p1;  // sequence and its page range [p0, p1)
   int slot;       // partial slot, or -1 when the segment is the whole sequence
-  int L;          // the sequence's length in tokens
 };
 
-// Enumerates the sequence segments of chunk k in order.  With a plan that
-// keeps whole sequences (mode 1: chunk k is sequence k) the one segment comes
-// straight from the sequence's length, which the caller has already loaded
-// (L_k, validated as the plan validates it), so a chunk starts without
-// reading the plan's prefix, edges or first-sequence table.
+// Enumerates the sequence segments of chunk k in order.
 struct ChunkIter {
   const int* prefix;
-  const int32_t* seqlens;
   int B, k, start, end, first_page, b;
-  int whole_L;  // mode 1: the length of sequence k; -1 otherwise
-  __device__ void init(const int* pf, const int* bounds, const int* cstart,
-                       const int32_t* lens, int B_, int k_, int mode, int L_k, int max_blocks) {
-    prefix = pf; seqlens = lens; B = B_; k = k_;
-    whole_L = -1;
-    if (mode == 1) {
-      const bool valid = L_k >= 0 && L_k <= max_blocks * kPage;
-      whole_L = valid ? L_k : 0;
-      start = 0;
-      end = (whole_L + kPage - 1) / kPage;
-      b = (start < end) ? k : B;
-      return;
-    }
+  __device__ void init(const int* pf, const int* bounds, const int* cstart, int B_, int k_) {
+    prefix = pf; B = B_; k = k_;
     start = bounds[k];
     end = bounds[k + 1];
     first_page = start;
@@ -445,20 +400,10 @@ struct ChunkIter {
   }
   __device__ bool next(Seg& s) {
     if (start >= end || b >= B) return false;
-    if (whole_L >= 0) {
-      s.b = b;
-      s.p0 = 0;
-      s.p1 = end;
-      s.slot = -1;
-      s.L = whole_L;
-      start = end;
-      return true;
-    }
     const int seg_end = min(end, prefix[b + 1]);
     s.b = b;
     s.p0 = start - prefix[b];
     s.p1 = seg_end - prefix[b];
-    s.L = seqlens[b];
     const int npages = prefix[b + 1] - prefix[b];
     const bool whole = (s.p0 == 0 && s.p1 == npages);
     const bool first = (start == first_page);
@@ -564,73 +509,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers are initialised before any remote store
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // Thread r (warps 0-3) puts its head's share of q[b] in place: the 256 c_kv
-  // columns into TMEM (A operand of the c_kv S MMAs), the 32 RoPE columns into
-  // shared memory (64-byte rows, 64-byte swizzle: 16-byte chunk c of row r at
-  // chunk c ^ ((r >> 1) & 3)).  All of the head's columns are in flight at
-  // once (one memory latency, not one per atom).
-  auto load_q = [&](int b, int r) {
-    const uint32_t tQ = tbase + ((uint32_t)((r >> 5) * 32) << 16) + kColQ;
-    const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)b * kHq + r) * kDk);
-    uint4 qv[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) qv[c] = __ldg(qrow + atom_col(0) / 8 + c);
-    uint4 qr[kRopeRowBytes / 16];
-#pragma unroll
-    for (int c = 0; c < kRopeRowBytes / 16; ++c) qr[c] = __ldg(qrow + rope_col / 8 + c);
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      uint32_t w[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = qv[a * 8 + c];
-        w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
-      }
-      tmem_st32(tQ + a * 32, w);
-    }
-    uint8_t* qs = smem + kQropeOff + r * kRopeRowBytes;
-#pragma unroll
-    for (int c = 0; c < kRopeRowBytes / 16; ++c)
-      *reinterpret_cast<uint4*>(qs + ((c ^ ((r >> 1) & 3)) * 16)) = qr[c];
-    fence_proxy_async_smem();
-    tmem_st_wait();
-  };
-  // While the plan kernel runs: a plan that keeps whole sequences gives
-  // cluster k sequence k, so its length is loaded now and what the sequence
-  // needs first is brought into L2 -- its block-table row, this CTA's share
-  // of its q rows and its first pages.  These are inputs of the call (the
-  // plan writes none of them, and the kernel before the plan has completed
-  // by the time this grid runs: the plan lets it start only after its own
-  // wait), so reading them here is safe; the page prefetches are hints whose
-  // block ids are bounds-checked first.  If the plan turns out to cut the
-  // sequences, the prefetched lines are simply not used.
-  const int guess_b = cluster < B ? cluster : -1;
-  const int L_guess = guess_b >= 0 ? seqlens[guess_b] : 0;
-  if (guess_b >= 0) {
-    if (warp == 4) {
-      const int32_t* trow = block_table + (size_t)guess_b * max_blocks;
-      for (int i = lane * 32; i < max_blocks; i += 32 * 32) prefetch_l2(trow + i);
-      const int npg = min((L_guess + kPage - 1) / kPage, kStages);
-      if (lane < npg && L_guess <= max_blocks * kPage) {
-        const int blk = trow[lane];
-        if (blk >= 0 && blk < num_blocks) {
-          for (int a = 0; a < 4; ++a) tma_prefetch_2d(&tmKV, atom_col(a), blk * kPage);
-          tma_prefetch_2d(&tmRope, rope_col, blk * kPage);
-        }
-      }
-    } else if (warp < 4) {
-      const __nv_bfloat16* qrow = q + ((size_t)guess_b * kHq + threadIdx.x) * kDk;
-#pragma unroll
-      for (int c = 0; c < 256; c += 64) prefetch_l2(qrow + atom_col(0) + c);
-      prefetch_l2(qrow + rope_col);
-    }
-  }
   // The set-up above overlaps the plan kernel; its chunk list is read only
   // now.  A cluster without a chunk runs no role loop and goes to teardown.
   grid_dependency_wait();
   grid_launch_dependents();  // the combine kernel may be scheduled
   const int nchunks = hdr[1];
-  const int mode = hdr[3];
 
   if (warp == 4) {
     // ================= producer: paged K/V (own columns) =================
@@ -642,11 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, bounds, cstart, seqlens, B, k, mode, mode == 1 ? (k == guess_b ? L_guess : seqlens[k]) : 0,
-                max_blocks);
+        it.init(prefix, bounds, cstart, B, k);
         Seg s;
         while (ok && it.next(s)) {
-          const int L = s.L;
+          const int L = seqlens[s.b];
           const int t_end = min(s.p1 * kPage, L);
           for (int t = s.p0 * kPage; t < t_end; t += kStep, ++g) {
             const int slot = g % kStages, use = g / kStages;
@@ -756,11 +638,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
-        it.init(prefix, bounds, cstart, seqlens, B, k, mode, mode == 1 ? (k == guess_b ? L_guess : seqlens[k]) : 0,
-                max_blocks);
+        it.init(prefix, bounds, cstart, B, k);
         Seg s;
         while (ok && it.next(s)) {
-          const int n = seg_steps(s.p0, s.p1, s.L);
+          const int n = seg_steps(s.p0, s.p1, seqlens[s.b]);
           ok = mbar_wait(bar_q_full, seg_i & 1, abort_flag, err, kSiteQFull, seg_i);
           if (!ok) break;
           tc_fence_after();
@@ -814,10 +695,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int total = 0;
     for (int k = cluster; k < nchunks; k += nclusters) {
       ChunkIter it;
-      it.init(prefix, bounds, cstart, seqlens, B, k, mode, mode == 1 ? (k == guess_b ? L_guess : seqlens[k]) : 0,
-              max_blocks);
+      it.init(prefix, bounds, cstart, B, k);
       Seg s;
-      while (it.next(s)) total += seg_steps(s.p0, s.p1, s.L);
+      while (it.next(s)) total += seg_steps(s.p0, s.p1, seqlens[s.b]);
     }
     for (int gg = 0; gg < total; ++gg) {
       const int sb = gg % kSBufs;
@@ -850,6 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;  // head == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tbase + lane_off + kColO;
+    const uint32_t tQ = tbase + lane_off + kColQ;
     const uint32_t tS0 = tbase + lane_off + kColS;
     const uint8_t* my_row = smem + kXOff + r * 16;  // this head's 16 B of each token quad
     constexpr float kLn2 = 0.69314718055994530942f;
@@ -898,11 +779,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     for (int k = cluster; k < nchunks && ok; k += nclusters) {
       ChunkIter it;
-      it.init(prefix, bounds, cstart, seqlens, B, k, mode, mode == 1 ? (k == guess_b ? L_guess : seqlens[k]) : 0,
-              max_blocks);
+      it.init(prefix, bounds, cstart, B, k);
       Seg s;
       while (ok && it.next(s)) {
-        const int L = s.L;
+        const int L = seqlens[s.b];
         const int t0 = s.p0 * kPage;
         const int n = seg_steps(s.p0, s.p1, L);
         // ---- this segment's q columns -> TMEM (A operand of the S MMAs)
@@ -911,9 +791,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
-        load_q(s.b, r);
-        tc_fence_before();
-        mbar_arrive(bar_q_full);
+        {
+          const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + r) * kDk);
+          // all of this head's 256 columns in flight at once (one memory
+          // latency per segment, not one per atom), then into TMEM
+          uint4 qv[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) qv[c] = __ldg(qrow + atom_col(0) / 8 + c);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = qv[a * 8 + c];
+              w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+            }
+            tmem_st32(tQ + a * 32, w);
+          }
+          {
+            // RoPE half -> shared memory, 64-byte rows with the 64-byte
+            // swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3))
+            uint8_t* qr = smem + kQropeOff + r * kRopeRowBytes;
+#pragma unroll
+            for (int c = 0; c < kRopeRowBytes / 16; ++c)
+              *reinterpret_cast<uint4*>(qr + ((c ^ ((r >> 1) & 3)) * 16)) =
+                  __ldg(qrow + rope_col / 8 + c);
+            fence_proxy_async_smem();
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar_q_full);
+        }
         // ---- the previous segment's epilogue overlaps this segment's first S
         if (prev_b >= 0) {
           ok = mbar_wait(bar_o_ready, prev_seg & 1, abort_flag, err, kSitePvDone, prev_seg);
@@ -1297,17 +1205,12 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   {
-    // The plan's CTA should share its SM with a decode CTA rather than hold
-    // that SM's shared memory split at a small carveout until it ends.
-    e = cudaFuncSetAttribute(mla_plan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
     cudaLaunchAttribute pdl1[1];
     pdl1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl1[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t pc = {};
     pc.gridDim = dim3(1, 1, 1);
-    pc.blockDim = dim3(kPlanThreads, 1, 1);
+    pc.blockDim = dim3(1024, 1, 1);
     pc.stream = s;
     pc.attrs = pdl1;
     pc.numAttrs = 1;

@@ -175,19 +175,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
 
 // --------------------------------------------------------------- TMA
 
-// Bring the 128-byte line holding p into L2 (no data returned, never faults).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
-}
-
-// Bring one tile of a tensor map into L2 (no shared-memory destination, no
-// barrier): cp.async.bulk.prefetch.tensor, 2-D tile mode.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-               ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m))
                : "memory");
