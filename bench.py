@@ -460,6 +460,31 @@ class LayerLeg(DecodeLeg):
     def workload_name(self):
         return "bf16 MLA layer (absorb + decode + project) batch64 Hq128 seq4096"
 
+    def tolerance(self):
+        # the layer's bounds: the absorbed query is itself rounded to bf16
+        # before the decode reads it, and the value projection rescales O
+        return {"o_rel_to_max_ref": 2e-2, "lse": 5e-3}
+
+    def oracle_check(self, threads: int, max_rows: int):
+        """The layer's output against attention over explicitly decompressed
+        keys and values (the definition before any absorption), on the first
+        two sequences, all heads: the fp64 oracle takes seconds per sequence."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n = 2
+        t0 = time.perf_counter()
+        ref, rl = oracle.mla_decompressed(self.qn[:n], self.qr[:n], self.wk, self.wv, self.kv,
+                                          self.table[:n], self.sl[:n], c.scale)
+        dt = time.perf_counter() - t0
+        got = self.out[:n].float().cpu().numpy()
+        gl = self.lse[:n].cpu().numpy()
+        rel = float(np.abs(got - ref).max() / np.abs(ref).max())
+        return {"o": rel, "lse": float(np.abs(gl - rl).max()), "rows": n * c.Hq,
+                "of_rows": c.batch * c.Hq, "tolerance": {"o": 2e-2, "lse": 5e-3},
+                "o_is_relative_to_max_ref": True, "oracle_s": dt,
+                "oracle_gbs": self.bytes * (n / c.batch) / dt / 1e9}
+
     def oracle_sample(self, budget_s: float, threads: int):
         import oracle
         c = self.cfg
