@@ -82,8 +82,9 @@ struct Cfg {
   static constexpr int kBarOff = kOutOff + kTilesPerCta * kAtomBytes;
   // barriers: q_full[tile], q_free[tile], kv_full[S], kv_empty[S], s_full[tile],
   // p_full[tile][half], pv_done[tile][half], o_free[tile], item_full[4],
-  // item_empty[4], mma_drain.  The per-half barriers each complete once per
-  // KV block, so no waiter is ever two phases behind or ahead of one.
+  // item_empty[4], mma_drain.  p_full[t][h] and pv_done[t][0] complete once
+  // per KV block and pv_done[t][1] once per item, so no waiter is ever two
+  // phases behind or ahead of one.
   static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 4 + 4 + 2 + 2 * kItemSlots + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, item ring
   static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
@@ -330,9 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // O_t += P_t V_j in two halves of 64 keys: the softmax of tile t hands
-      // each half h of P_t over on p_full[t][h], and that half's MMAs are
-      // committed to pv_done[t][h] (each completes once per block).
-      auto issue_pv = [&](auto tile, int j) -> bool {
+      // each half h of P_t over on p_full[t][h].  The first half's MMAs are
+      // committed to pv_done[t][0] every block (the second half's rescale of
+      // O waits for them); the second half's only on the tile's last block of
+      // the item, for the epilogue (pv_done[t][1] completes once per item).
+      // Within an item nothing else needs the second half: S_t(j+1) is issued
+      // after PV_t(j), and a commit covers every earlier MMA of this thread,
+      // so s_full[t] of block j+1 already implies PV_t(j) is done.  The steady
+      // loop, which never holds a last block, passes NotLast and skips the
+      // test.
+      using MaybeLast = std::true_type;
+      using NotLast = std::false_type;
+      auto issue_pv = [&](auto tile, int j, auto may_be_last) -> bool {
         constexpr int t = decltype(tile)::value;
         const int x = kv + j;
         const int slot = x % C::kStages;
@@ -353,7 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
                    kk > 0 ? 1u : acc0);
           }
-          tc_commit(bar_pv_done(t, h));
+          if (h == 0) {
+            tc_commit(bar_pv_done(t, 0));
+          } else if constexpr (decltype(may_be_last)::value) {
+            if (j == (t ? T1 : T0) - 1) tc_commit(bar_pv_done(t, 1));
+          }
         }
         // the stage of block j is free once the last tile reading it is done
         if (t == 1 || j >= T1) tc_commit(bar_kv_empty(slot));
@@ -401,12 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // then loads the next item's Q_t while this item's tail still runs.
         if (ok && T0 == 1) tc_commit(bar_q_free(0));
         if (ok && T1 == 1) tc_commit(bar_q_free(1));
-        if (ok) ok = wait_o_free(Tile0{}) && issue_pv(Tile0{}, 0);
+        if (ok) ok = wait_o_free(Tile0{}) && issue_pv(Tile0{}, 0, MaybeLast{});
         if (ok && T0 > 1) {
           ok = issue_s(Tile0{}, 1, Wait{});
           if (ok && T0 == 2) tc_commit(bar_q_free(0));
         }
-        if (ok && T1 > 0) ok = wait_o_free(Tile1{}) && issue_pv(Tile1{}, 0);
+        if (ok && T1 > 0) ok = wait_o_free(Tile1{}) && issue_pv(Tile1{}, 0, MaybeLast{});
         if (ok && T1 > 1) {
           ok = issue_s(Tile1{}, 1, Wait{});
           if (ok && T1 == 2) tc_commit(bar_q_free(1));
@@ -418,22 +432,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         int j = 1;
         if (T1 > 0) {
           for (; j < j_tail && ok; ++j) {
-            ok = issue_pv(Tile0{}, j);
+            ok = issue_pv(Tile0{}, j, NotLast{});
             if (ok) ok = issue_s(Tile0{}, j + 1, Wait{});
-            if (ok) ok = issue_pv(Tile1{}, j);
+            if (ok) ok = issue_pv(Tile1{}, j, NotLast{});
             if (ok) ok = issue_s(Tile1{}, j + 1, NoWait{});
           }
         }
         for (; j < Tmax && ok; ++j) {
           if (j < T0) {
-            ok = issue_pv(Tile0{}, j);
+            ok = issue_pv(Tile0{}, j, MaybeLast{});
             if (ok && j + 1 < T0) {
               ok = issue_s(Tile0{}, j + 1, Wait{});
               if (ok && j + 2 == T0) tc_commit(bar_q_free(0));
             }
           }
           if (ok && j < T1) {
-            ok = issue_pv(Tile1{}, j);
+            ok = issue_pv(Tile1{}, j, MaybeLast{});
             if (ok && j + 1 < T1) {
               ok = issue_s(Tile1{}, j + 1, Wait{});
               if (ok && j + 2 == T1) tc_commit(bar_q_free(1));
@@ -461,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tbase + lane_off + C::kColO + t * 128;
     const uint32_t stage_addr = base + C::kOutOff + t * kAtomBytes;  // this tile's O staging
     uint8_t* stage = smem + C::kOutOff + t * kAtomBytes;
-    int bc = 0;  // KV blocks this tile has been through (barrier phases)
+    int bc = 0;   // KV blocks this tile has been through (barrier phases)
+    int nit = 0;  // items this tile has been through (pv_done[t][1] phases)
 
     for (int k = 0;; ++k) {
       const int islot = k % kItemSlots;
@@ -613,15 +628,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
           // Lazy correction of O before this half's PV: needed only if some row
           // of this warp moved its reference, and only once every earlier PV of
-          // the tile has landed: the second half of block j-1 (h = 0) or the
-          // first half of block j (h = 1).
+          // the tile has landed.  For h = 0 that is block j-1's PV, already
+          // complete when s_full of block j was seen (S_t(j) was issued after
+          // it, and a commit covers every earlier MMA); for h = 1 it is the
+          // first half of block j, signalled on pv_done[t][0].
           if ((j > 0 || h > 0) && __any_sync(0xffffffffu, resc)) {
-            ok = h == 0 ? mbar_wait(bar_pv_done(t, 1), (bc + j - 1) & 1, abort_flag, err,
-                                    kSitePvDone, 2 * j)
-                        : mbar_wait(bar_pv_done(t, 0), (bc + j) & 1, abort_flag, err, kSitePvDone,
-                                    2 * j + 1);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            if (h == 1) {
+              ok = mbar_wait(bar_pv_done(t, 0), (bc + j) & 1, abort_flag, err, kSitePvDone,
+                             2 * j + 1);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+            }
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -645,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile's staging buffer, each stored by TMA; LSE.  All four warps of the
       // warpgroup reach every barrier below on every path (their waits are
       // bounded); stores are skipped once any role has aborted.
-      if (ok) ok = mbar_wait(bar_pv_done(t, 1), (bc + T - 1) & 1, abort_flag, err, kSitePvDone, 2 * T);
+      if (ok) ok = mbar_wait(bar_pv_done(t, 1), nit & 1, abort_flag, err, kSitePvDone, 2 * T);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -689,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse[(size_t)bh * N + row] = (m_ref + log2f(l)) * kLn2;
       }
       bc += T;
+      ++nit;
       // one decision for the whole warpgroup: go on to the next item or stop
       if (named_barrier_any(1 + t, 128, !ok || *abort_flag != 0)) break;
     }
