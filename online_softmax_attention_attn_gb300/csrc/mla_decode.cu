@@ -26,9 +26,8 @@
 //     identical softmax; each CTA accumulates its 256 columns of O = P V in
 //     TMEM (V is the same shared-memory bytes as K).
 //   * Each 64-token page is one step (S MMAs with N=64) through a 4-stage TMA
-//     ring of the CTA's c_kv atoms (rank 0's RoPE atom has a 2-slot ring of its
-//     own, freed as soon as S completes); the block table is read on the
-//     device and bounds-checked.  Two S
+//     ring of the CTA's c_kv atoms and its 32 RoPE columns; the block table is
+//     read on the device and bounds-checked.  Two S
 //     buffers in TMEM let the tensor core compute step g+1 while the softmax
 //     of step g runs; the partial S travels in two 32-token halves.  Warps:
 //     0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer, 6-9 partial-S
@@ -60,9 +59,11 @@ constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
 constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
 constexpr int kStages = 4;
 // The 64 RoPE columns are split between the ranks, 32 each (64-byte rows,
-// 64-byte swizzle).  They are read by the S MMAs only, so they have a ring of
-// their own that is released when S completes (much earlier than PV).
-constexpr int kRopeSlots = 2;
+// 64-byte swizzle).  Each stage has a RoPE slot of its own beside its c_kv
+// atoms, loaded and released with the stage (released by the stage's PV
+// commit: a separate early release after S would cost the MMA-issuing thread
+// one more commit per step).
+constexpr int kRopeSlots = kStages;
 constexpr int kRopeCols = 32;                       // RoPE columns per CTA
 constexpr int kRopeRowBytes = kRopeCols * 2;        // 64 B
 constexpr int kQropeBytes = kHq * kRopeRowBytes;    // q's RoPE half: 8 KB
@@ -89,8 +90,7 @@ constexpr int kXOff = kStageOff + kStages * kStageBytes;
 constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
 // barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], s_read[2],
 // xfull[4], b_read[2], q_full, q_free, pv_done, o_free, mma_drain, o_ready,
-// rope_empty[2]
-constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6 + kRopeSlots;
+constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -468,7 +468,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // epilogue waits on it (pv_done completes once per step and may lag by more
   // than one phase at that point, so its parity would be ambiguous there).
   const uint32_t bar_o_ready = bar_q_full + 40;
-  auto bar_rope_empty = [&](int r) { return bar_q_full + 48 + 8u * r; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -492,7 +491,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar_o_free, 128);
     mbar_init(bar_mma_drain, 1);
     mbar_init(bar_o_ready, 1);
-    for (int r = 0; r < kRopeSlots; ++r) mbar_init(bar_rope_empty(r), 1);
     *abort_flag = 0;
     fence_mbar_init();
     // arm the receive barriers for half steps 0..3 (re-armed after each use)
@@ -536,12 +534,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
               if (!ok) break;
             }
-            const int rslot = g % kRopeSlots, ruse = g / kRopeSlots;
-            if (ruse > 0) {
-              ok = mbar_wait(bar_rope_empty(rslot), (ruse - 1) & 1, abort_flag, err, kSiteKvEmpty,
-                             g);
-              if (!ok) break;
-            }
             if (g == skip_step) {
               skipped = g;
               issued = g + 1;
@@ -554,13 +546,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const int row = blk * kPage + (t % kPage);
             const uint32_t dst = sStage + slot * kStageBytes;
-            // the c_kv atoms into the stage and the RoPE half into its own
-            // ring, all counted on the stage's full barrier
+            // the c_kv atoms and the RoPE half into the stage, all counted on
+            // the stage's full barrier
             mbar_arrive_expect_tx(bar_kv_full(slot), 4 * kKAtomBytes + kKropeBytes);
             for (int a = 0; a < 4; ++a)
               tma_load_2d_hint(dst + a * kKAtomBytes, &tmKV, bar_kv_full(slot), atom_col(a), row,
                                pol_kv);
-            tma_load_2d_hint(sRope + rslot * kKropeBytes, &tmRope, bar_kv_full(slot), rope_col, row,
+            tma_load_2d_hint(sRope + slot * kKropeBytes, &tmRope, bar_kv_full(slot), rope_col, row,
                              pol_kv);
             issued = g + 1;
           }
@@ -608,18 +600,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    kIdescS, (a | kk) != 0);
         }
         {
-          const uint64_t rd = kropedesc0 + (uint64_t)(((u & (kRopeSlots - 1)) * kKropeBytes) >> 4);
+          const uint64_t rd = kropedesc0 + (uint64_t)((slot * kKropeBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kRopeCols / 16; ++kk)
             mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
                    kIdescS, 1u);
         }
         tc_commit(bar_s_full(u & (kSBufs - 1)));
-        tc_commit(bar_rope_empty(u & (kRopeSlots - 1)));  // the RoPE slot is free
         return true;
       };
       // O[:, own columns] += P V for global step gg (P in TMEM over its S)
-      auto issue_pv = [&](int gg, uint32_t acc_first) -> bool {
+      // O[:, own columns] += P V for global step gg.  pv_done is committed only
+      // after the PV of a segment's second-to-last step: the O rescale of any
+      // earlier step waits for the next step's S instead (issued after this
+      // PV, and a commit covers every earlier MMA of this thread).
+      auto issue_pv = [&](int gg, uint32_t acc_first, bool commit_done) -> bool {
         const uint32_t u = (uint32_t)gg;
         const uint32_t sb = u & (kSBufs - 1);
         const uint32_t slot = u & (kStages - 1);
@@ -633,7 +628,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kk = 1; kk < kStep / 16; ++kk)
           mma_ts(tO, aP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
         tc_commit(bar_kv_empty(slot));
-        tc_commit(bar_pv_done);
+        if (commit_done) tc_commit(bar_pv_done);
         return true;
       };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
@@ -655,18 +650,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // is never the segment's last, then a tail of at most three steps
           // that carries the hand-over commits: no branches in the steady
           // part, where every instruction of this thread delays the pipe
-          if (ok) ok = issue_pv(g, 0u);
+          if (ok) ok = issue_pv(g, 0u, n == 2);
           if (ok && n > kSBufs) {
             ok = issue_s(g + kSBufs);
             if (ok && n == kSBufs + 1) tc_commit(bar_q_free);
           }
           int i = 1;
           for (; i + kSBufs + 1 < n && ok; ++i) {
-            ok = issue_pv(g + i, 1u);
+            ok = issue_pv(g + i, 1u, false);
             if (ok) ok = issue_s(g + i + kSBufs);
           }
           for (; i < n && ok; ++i) {
-            ok = issue_pv(g + i, 1u);
+            ok = issue_pv(g + i, 1u, i == n - 2);
             if (ok && i + kSBufs < n) {
               ok = issue_s(g + i + kSBufs);
               if (ok && i + kSBufs == n - 1) tc_commit(bar_q_free);
@@ -735,6 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint8_t* my_row = smem + kXOff + r * 16;  // this head's 16 B of each token quad
     constexpr float kLn2 = 0.69314718055994530942f;
     int g = 0, seg_i = 0;
+    int pvd = 0;  // pv_done phases completed before this segment
     bool ok = true;
     // the previous segment, whose epilogue runs once the next q is in place
     int prev_b = -1, prev_slot = -1, prev_seg = 0;
@@ -979,8 +975,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
           }
+          // O is rescaled once the previous step's PV is done: seen through
+          // the next step's S (issued after that PV), or, at a segment's last
+          // step, through pv_done (committed once per segment of two or more
+          // steps, after the PV of its second-to-last step).
           if (i > 0 && __any_sync(0xffffffffu, resc)) {
-            ok = mbar_wait(bar_pv_done, (gi - 1) & 1, abort_flag, err, kSitePvDone, gi);
+            if (i + 1 < n) {
+              const int gn = gi + 1;
+              ok = mbar_wait(bar_s_full(gn % kSBufs), (gn / kSBufs) & 1, abort_flag, err,
+                             kSitePvDone, gi);
+            } else {
+              ok = mbar_wait(bar_pv_done, pvd & 1, abort_flag, err, kSitePvDone, gi);
+            }
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -1010,6 +1016,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prev_seg = seg_i;
         prev_m = m_ref;
         prev_l = l;
+        if (n >= 2) ++pvd;
         g += n;
         ++seg_i;
       }
