@@ -81,10 +81,10 @@ struct Cfg {
   static constexpr int kOutOff = kRingOff + kStages * kStageBytes;  // O staging, one atom per tile
   static constexpr int kBarOff = kOutOff + kTilesPerCta * kAtomBytes;
   // barriers: q_full[tile], q_free[tile], kv_full[S], kv_empty[S], s_full[tile],
-  // p_full[tile][half], pv_done[tile][half], o_free[tile], item_full[4],
-  // item_empty[4], mma_drain.  p_full[t][h] and pv_done[t][0] complete once
-  // per KV block and pv_done[t][1] once per item, so no waiter is ever two
-  // phases behind or ahead of one.
+  // p_full[tile] (+1 unused), pv_done[tile] (+1 unused), o_free[tile],
+  // item_full[4], item_empty[4], mma_drain.  p_full[t] completes once per KV
+  // block and pv_done[t] once per item, so no waiter is ever two phases
+  // behind or ahead of one.
   static constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 4 + 4 + 2 + 2 * kItemSlots + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, item ring
   static constexpr int kSmemBytes = kMiscOff + 32 + 1024;  // + alignment slack
@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
   auto bar_kv_empty = [&](int s) { return bar0 + 8u * (4 + C::kStages + s); };
   auto bar_s_full = [&](int t) { return bar0 + 8u * (4 + 2 * C::kStages + t); };
-  auto bar_p_full = [&](int t, int h) { return bar0 + 8u * (6 + 2 * C::kStages + 2 * t + h); };
-  auto bar_pv_done = [&](int t, int h) { return bar0 + 8u * (10 + 2 * C::kStages + 2 * t + h); };
+  auto bar_p_full = [&](int t) { return bar0 + 8u * (6 + 2 * C::kStages + t); };
+  auto bar_pv_done = [&](int t) { return bar0 + 8u * (10 + 2 * C::kStages + t); };
   auto bar_o_free = [&](int t) { return bar0 + 8u * (14 + 2 * C::kStages + t); };
   auto bar_item_full = [&](int i) { return bar0 + 8u * (16 + 2 * C::kStages + i); };
   auto bar_item_empty = [&](int i) {
@@ -170,10 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_q_free(t), 1);
       mbar_init(bar_s_full(t), 1);
       mbar_init(bar_o_free(t), 128);
-      for (int h = 0; h < 2; ++h) {
-        mbar_init(bar_p_full(t, h), 128);
-        mbar_init(bar_pv_done(t, h), 1);
-      }
+      mbar_init(bar_p_full(t), 128);
+      mbar_init(bar_pv_done(t), 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
@@ -330,16 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar_s_full(t));
         return true;
       };
-      // O_t += P_t V_j in two halves of 64 keys: the softmax of tile t hands
-      // each half h of P_t over on p_full[t][h].  The first half's MMAs are
-      // committed to pv_done[t][0] every block (the second half's rescale of
-      // O waits for them); the second half's only on the tile's last block of
-      // the item, for the epilogue (pv_done[t][1] completes once per item).
-      // Within an item nothing else needs the second half: S_t(j+1) is issued
-      // after PV_t(j), and a commit covers every earlier MMA of this thread,
-      // so s_full[t] of block j+1 already implies PV_t(j) is done.  The steady
-      // loop, which never holds a last block, passes NotLast and skips the
-      // test.
+      // O_t += P_t V_j: the softmax of tile t hands the block's P over on
+      // p_full[t].  pv_done[t] is committed only after the tile's last block
+      // of an item, for the epilogue: within an item the next block's S
+      // commit already covers this PV (a commit tracks every earlier MMA of
+      // this thread).  The steady loop, which never holds a last block,
+      // passes NotLast and skips the test.
       using MaybeLast = std::true_type;
       using NotLast = std::false_type;
       auto issue_pv = [&](auto tile, int j, auto may_be_last) -> bool {
@@ -351,23 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dO = tbase + C::kColO + t * 128;
         const uint32_t aP = tbase + C::kColS + t * 128;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
+        if (!mbar_wait(bar_p_full(t), ph, abort_flag, err, kSitePFull, j)) return false;
+        tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(bar_p_full(t, h), ph, abort_flag, err, kSitePFull, 2 * j + h))
-            return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
-            // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
-            // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
-            mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                   kk > 0 ? 1u : acc0);
-          }
-          if (h == 0) {
-            tc_commit(bar_pv_done(t, 0));
-          } else if constexpr (decltype(may_be_last)::value) {
-            if (j == (t ? T1 : T0) - 1) tc_commit(bar_pv_done(t, 1));
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          // A = P (bf16, 2 per TMEM column): keys [16kk, 16kk+16) = 8 columns.
+          // B = V block, MN-major: 16 keys = 2 groups of 8 rows of 128 B.
+          mma_ts(dO, aP + kk * 8, vb + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                 kk > 0 ? 1u : acc0);
+        }
+        if constexpr (decltype(may_be_last)::value) {
+          if (j == (t ? T1 : T0) - 1) tc_commit(bar_pv_done(t));
         }
         // the stage of block j is free once the last tile reading it is done
         if (t == 1 || j >= T1) tc_commit(bar_kv_empty(slot));
@@ -503,9 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
         if (!ok) break;
         tc_fence_after();
-        // Each 64-key half of the block is an online-softmax step of its own:
-        // its P is handed to the MMA thread as soon as it is written, so the PV
-        // MMAs of the first half run while the second half is computed.
+        // Each 64-key half of the block is an online-softmax step of its own
+        // (its own fast-path bound and, if needed, exact max); the block's P is
+        // handed to the MMA thread once, after both halves, which keeps the
+        // MMA thread's waits and commits to one each per tile and block.
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           const int nvalid = lim - j * kBN - h * 64;  // keys c < nvalid of this half are visible
@@ -626,34 +615,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             l += (r0 + r1) + (r2 + r3);
           }
 
-          // Lazy correction of O before this half's PV: needed only if some row
-          // of this warp moved its reference, and only once every earlier PV of
-          // the tile has landed.  For h = 0 that is block j-1's PV, already
-          // complete when s_full of block j was seen (S_t(j) was issued after
-          // it, and a commit covers every earlier MMA); for h = 1 it is the
-          // first half of block j, signalled on pv_done[t][0].
-          if ((j > 0 || h > 0) && __any_sync(0xffffffffu, resc)) {
-            if (h == 1) {
-              ok = mbar_wait(bar_pv_done(t, 0), (bc + j) & 1, abort_flag, err, kSitePvDone,
-                             2 * j + 1);
-              ok = __all_sync(0xffffffffu, ok);
-              if (!ok) break;
-            }
-            tc_fence_after();
+          // Lazy correction when some row of this warp moved its reference:
+          // O holds every PV up to block j-1, already complete when s_full of
+          // block j was seen (S_t(j) was issued after it, and a commit covers
+          // every earlier MMA), so it is rescaled without a wait; and in the
+          // second half the first half's P, written but not yet handed over,
+          // is rescaled in TMEM too (one more bf16 rounding, on this rare path).
+          if (__any_sync(0xffffffffu, resc)) {
+            if (j > 0) {
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              float ov[32];
-              tmem_ld32(tO + c * 32, ov);
-              uint32_t ou[32];
+              for (int c = 0; c < D / 32; ++c) {
+                float ov[32];
+                tmem_ld32(tO + c * 32, ov);
+                uint32_t ou[32];
 #pragma unroll
-              for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
-              tmem_st32(tO + c * 32, ou);
+                for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
+                tmem_st32(tO + c * 32, ou);
+              }
+            }
+            if (h == 1) {
+              tmem_st_wait();  // the first half's P is in place before it is read back
+              uint32_t pw[32];
+              tmem_ld32(tS, reinterpret_cast<float*>(pw));
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const float2 f = unpack_bf16x2(pw[u]);
+                pw[u] = pack_bf16x2(f.x * alpha, f.y * alpha);
+              }
+              tmem_st32(tS, pw);
             }
           }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar_p_full(t, h));
         }
+        // the whole block's P goes to the MMA thread in one hand-over
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_p_full(t));
 
         if (!ok) break;
       }
@@ -662,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile's staging buffer, each stored by TMA; LSE.  All four warps of the
       // warpgroup reach every barrier below on every path (their waits are
       // bounded); stores are skipped once any role has aborted.
-      if (ok) ok = mbar_wait(bar_pv_done(t, 1), nit & 1, abort_flag, err, kSitePvDone, 2 * T);
+      if (ok) ok = mbar_wait(bar_pv_done(t), nit & 1, abort_flag, err, kSitePvDone, 2 * T);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) tc_fence_after();
       const float inv_l = 1.0f / l;
