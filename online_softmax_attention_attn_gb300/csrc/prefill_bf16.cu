@@ -303,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The tile is a compile-time constant so that the issue path carries
       // no per-tile selects: every instruction of this thread delays the pipe.
       // Where the other tile's S of the same block was issued just before
-      // (the steady part), the stage is known to be full and the wait is
-      // left out.
+      // (tile 1's S of any block that tile 0 also visits), the stage is known
+      // to be full and the wait is left out.
       using Wait = std::true_type;
       using NoWait = std::false_type;
       auto issue_s = [&](auto tile, int j, auto wait) -> bool {
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar_q_full(1), qn1 & 1, abort_flag, err, kSiteQFull, k);
           if (ok) {
             tc_fence_after();
-            ok = issue_s(Tile1{}, 0, Wait{});
+            ok = issue_s(Tile1{}, 0, NoWait{});  // tile 0's S of block 0 waited
           }
         }
         // q_free[t] is committed right after the tile's last S: the producer
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && T1 > 0) ok = wait_o_free(Tile1{}) && issue_pv(Tile1{}, 0, MaybeLast{});
         if (ok && T1 > 1) {
-          ok = issue_s(Tile1{}, 1, Wait{});
+          ok = T0 > 1 ? issue_s(Tile1{}, 1, NoWait{}) : issue_s(Tile1{}, 1, Wait{});
           if (ok && T1 == 2) tc_commit(bar_q_free(1));
         }
         // blocks 1.. : the steady part has no last S of either tile and so
@@ -437,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && j < T1) {
             ok = issue_pv(Tile1{}, j, MaybeLast{});
             if (ok && j + 1 < T1) {
-              ok = issue_s(Tile1{}, j + 1, Wait{});
+              ok = j + 1 < T0 ? issue_s(Tile1{}, j + 1, NoWait{})
+                              : issue_s(Tile1{}, j + 1, Wait{});
               if (ok && j + 2 == T1) tc_commit(bar_q_free(1));
             }
           }
