@@ -53,16 +53,18 @@ constexpr int kDk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
 constexpr int kStep = 64;                 // tokens per MMA step (one page)
-constexpr int kHalf = 32;                 // tokens per partial-S exchange
-constexpr int kThreads = 320;             // softmax, producer, MMA, exchange warps
+constexpr int kHalf = 32;                 // tokens per softmax warp and per partial-S message
+constexpr int kOwn = kHq / 2;             // heads whose softmax runs on each CTA
+// Warps 0-7 compute (warp w: TMEM lane quarter w % 4, token half / column
+// half w / 4; the softmax for this CTA's 64 heads, or the partial-S sends and
+// O upkeep for the peer's 64), 8 TMA producer, 9 S-MMA issuer, 10 PV-MMA issuer.
+constexpr int kThreads = 352;
 constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
 constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
 constexpr int kStages = 4;
 // The 64 RoPE columns are split between the ranks, 32 each (64-byte rows,
 // 64-byte swizzle).  Each stage has a RoPE slot of its own beside its c_kv
-// atoms, loaded and released with the stage (released by the stage's PV
-// commit: a separate early release after S would cost the MMA-issuing thread
-// one more commit per step).
+// atoms, loaded and released with the stage.
 constexpr int kRopeSlots = kStages;
 constexpr int kRopeCols = 32;                       // RoPE columns per CTA
 constexpr int kRopeRowBytes = kRopeCols * 2;        // 64 B
@@ -72,14 +74,26 @@ constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 static_assert((kStages & (kStages - 1)) == 0 && (kSBufs & (kSBufs - 1)) == 0 &&
                   (kRopeSlots & (kRopeSlots - 1)) == 0,
               "ring positions are taken with masks");
-constexpr int kXBufs = 4;                 // partial-S receive half-buffers (2 steps)
-// A received half is [token quad q][head][4 tokens] fp32: 16 B per head and
-// quad, so one exchange-warp store covers 512 contiguous bytes (32 heads) --
-// contiguous remote stores move about twice the bytes per clock of
-// row-scattered ones -- and each head's reads are conflict-free.
-constexpr int kXQuadBytes = kHq * 16;          // one token quad, all heads
-constexpr int kXBufBytes = (kHalf / 4) * kXQuadBytes;
-constexpr uint32_t kXBytes = kXBufBytes;       // payload per half step
+// A partial-S message: one token half of one step for the 64 heads of the
+// receiving CTA, [token quad][head][4 tokens] fp32: 16 B per head and quad, so
+// one warp store covers 512 contiguous bytes (contiguous remote stores move
+// about twice the bytes per clock of row-scattered ones) and each head's
+// reads are conflict-free.
+constexpr int kXQuadBytes = kOwn * 16;                 // 1 KB
+constexpr int kXMsgBytes = (kHalf / 4) * kXQuadBytes;  // 8 KB
+constexpr int kXSlots = 2 * 2;                         // two steps x two token halves
+// P of one step in shared memory (the A operand of the PV MMAs): two K-major
+// atoms of 32 tokens (64-byte rows, 64-byte swizzle) over the 128 head rows.
+// A warp's 32 rows of one atom are 2 KB contiguous, which is what it copies
+// to the peer.
+constexpr int kPAtomBytes = kHq * 64;         // 8 KB
+constexpr int kPSlotBytes = 2 * kPAtomBytes;  // 16 KB
+constexpr int kPSlots = 2;
+constexpr int kPWarpBytes = 32 * 64;          // 2 KB
+// per step each CTA receives the P rows of the peer's 64 heads and their
+// rescale factors; per segment their final row sums
+constexpr uint32_t kXpBytes = 4 * kPWarpBytes + kOwn * 4;
+constexpr uint32_t kLfinBytes = kOwn * 4;
 constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kQropeOff = 0;             // q's RoPE half (A of 2 S MMAs)
@@ -87,11 +101,17 @@ constexpr int kRopeOff = kQropeOff + kQropeBytes;  // k_rope ring
 constexpr int kStageOff = kRopeOff + kRopeSlots * kKropeBytes;
 static_assert(kStageOff % 1024 == 0, "swizzled stages start on 1024-byte boundaries");
 constexpr int kXOff = kStageOff + kStages * kStageBytes;
-constexpr int kBarOff = kXOff + kXBufs * kXBufBytes;
-// barriers: kv_full[S], kv_empty[S], s_full[2], p_full[2], s_read[2],
-// xfull[4], b_read[2], q_full, q_free, pv_done, o_free, mma_drain, o_ready,
-constexpr int kNumBars = 2 * kStages + 3 * kSBufs + kXBufs + kSBufs + 6;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kPOff = kXOff + kXSlots * kXMsgBytes;
+static_assert(kPOff % 1024 == 0, "P atoms start on swizzle-pattern boundaries");
+constexpr int kAlphaOff = kPOff + kPSlots * kPSlotBytes;  // [P slot][64] factors from the peer
+constexpr int kLfinOff = kAlphaOff + kPSlots * kOwn * 4;   // [segment parity][64] from the peer
+constexpr int kPmaxOff = kLfinOff + 2 * kOwn * 4;          // [step parity][half][64] row maxima
+constexpr int kLpartOff = kPmaxOff + 2 * 2 * kOwn * 4;     // [half][64] row sums
+constexpr int kBarOff = kLpartOff + 2 * kOwn * 4;
+// barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[4], x_read[4],
+// p_full[2], xp_full[2], lfin_full[2], q_full, q_free, o_free, drain_s, drain_pv
+constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 2 * kXSlots + 3 * kPSlots + 5;
+constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // 256 columns
@@ -451,23 +471,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t sRope = base + kRopeOff;
   const uint32_t sStage = base + kStageOff;
   const uint32_t sX = base + kXOff;
+  const uint32_t sP = base + kPOff;
   const uint32_t bar0 = base + kBarOff;
+  constexpr int kBarX = 2 * kStages + 2 * kSBufs;
+  constexpr int kBarP = kBarX + 2 * kXSlots;
   auto bar_kv_full = [&](int s) { return bar0 + 8u * s; };
-  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  // kv_free(s) completes when the PV of the stage's step is done on BOTH CTAs
+  // (each PV commit is multicast): it frees the stage for the producer, the P
+  // slot of the step two later, and it is how the O rescales and the
+  // epilogue learn that a PV is done.
+  auto bar_kv_free = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto bar_s_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto bar_p_full = [&](int b) { return bar0 + 8u * (2 * kStages + kSBufs + b); };
-  auto bar_s_read = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kSBufs + b); };
-  auto bar_xfull = [&](int b) { return bar0 + 8u * (2 * kStages + 3 * kSBufs + b); };
-  auto bar_b_read = [&](int b) { return bar0 + 8u * (2 * kStages + 3 * kSBufs + kXBufs + b); };
-  const uint32_t bar_q_full = bar0 + 8u * (2 * kStages + 3 * kSBufs + kXBufs + kSBufs);
+  auto bar_s_read = [&](int b) { return bar0 + 8u * (2 * kStages + kSBufs + b); };
+  auto bar_x_full = [&](int x) { return bar0 + 8u * (kBarX + x); };
+  auto bar_x_read = [&](int x) { return bar0 + 8u * (kBarX + kXSlots + x); };
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (kBarP + b); };
+  auto bar_xp_full = [&](int b) { return bar0 + 8u * (kBarP + kPSlots + b); };
+  auto bar_lfin_full = [&](int b) { return bar0 + 8u * (kBarP + 2 * kPSlots + b); };
+  const uint32_t bar_q_full = bar0 + 8u * (kBarP + 3 * kPSlots);
   const uint32_t bar_q_free = bar_q_full + 8;
-  const uint32_t bar_pv_done = bar_q_full + 16;
-  const uint32_t bar_o_free = bar_q_full + 24;
-  const uint32_t bar_mma_drain = bar_q_full + 32;
-  // o_ready completes once per segment, after that segment's last PV: the
-  // epilogue waits on it (pv_done completes once per step and may lag by more
-  // than one phase at that point, so its parity would be ambiguous there).
-  const uint32_t bar_o_ready = bar_q_full + 40;
+  const uint32_t bar_o_free = bar_q_full + 16;
+  const uint32_t bar_drain_s = bar_q_full + 24;
+  const uint32_t bar_drain_pv = bar_q_full + 32;
+  static_assert(kBarP + 3 * kPSlots + 5 == kNumBars, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -476,35 +502,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);
+      mbar_init(bar_kv_free(s), 2);
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar_s_full(b), 1);
-      mbar_init(bar_p_full(b), 128);
-      mbar_init(bar_s_read(b), 128);
+      mbar_init(bar_s_read(b), 8);  // every compute warp reads every S
     }
-    for (int b = 0; b < kXBufs; ++b) mbar_init(bar_xfull(b), 1);
-    for (int b = 0; b < kSBufs; ++b) mbar_init(bar_b_read(b), 128);
-    mbar_init(bar_q_full, 128);
+    for (int x = 0; x < kXSlots; ++x) {
+      mbar_init(bar_x_full(x), 1);
+      mbar_init(bar_x_read(x), 2);  // the two softmax warps of the half
+    }
+    for (int b = 0; b < kPSlots; ++b) {
+      mbar_init(bar_p_full(b), 8);
+      mbar_init(bar_xp_full(b), 1);
+      mbar_init(bar_lfin_full(b), 1);
+    }
+    mbar_init(bar_q_full, 8);
     mbar_init(bar_q_free, 1);
-    mbar_init(bar_pv_done, 1);
-    mbar_init(bar_o_free, 128);
-    mbar_init(bar_mma_drain, 1);
-    mbar_init(bar_o_ready, 1);
+    mbar_init(bar_o_free, 8);
+    mbar_init(bar_drain_s, 1);
+    mbar_init(bar_drain_pv, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // arm the receive barriers for half steps 0..3 (re-armed after each use)
-    for (int b = 0; b < kXBufs; ++b) mbar_arrive_expect_tx(bar_xfull(b), kXBytes);
+    // arm the barriers that count the peer's bytes (re-armed after each use)
+    for (int x = 0; x < kXSlots; ++x) mbar_arrive_expect_tx(bar_x_full(x), kXMsgBytes);
+    for (int b = 0; b < kPSlots; ++b) {
+      mbar_arrive_expect_tx(bar_xp_full(b), kXpBytes);
+      mbar_arrive_expect_tx(bar_lfin_full(b), kLfinBytes);
+    }
     prefetch_tmap(&tmKV);
     prefetch_tmap(&tmRope);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any remote store
+  cluster_sync();  // the peer's barriers are initialised before any remote access
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // The set-up above overlaps the plan kernel; its chunk list is read only
@@ -513,7 +548,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   grid_launch_dependents();  // the combine kernel may be scheduled
   const int nchunks = hdr[1];
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ================= producer: paged K/V (own columns) =================
     if (lane == 0) {
       const uint64_t pol_kv = policy_evict_first();  // every cached row is read once
@@ -531,7 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int t = s.p0 * kPage; t < t_end; t += kStep, ++g) {
             const int slot = g % kStages, use = g / kStages;
             if (use > 0) {
-              ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
+              ok = mbar_wait(bar_kv_free(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
               if (!ok) break;
             }
             if (g == skip_step) {
@@ -568,69 +603,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ================= MMA issuer =================
+  } else if (warp == 9) {
+    // ================= S issuer: partial S over this CTA's columns ==========
+    // S of a step needs only its stage and a free S buffer (P lives in shared
+    // memory), so this thread runs ahead of the PVs.
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(kHq, kStep, false, false);  // N = 64 tokens
-      constexpr uint32_t kIdescPV = idesc_bf16(kHq, 256, false, true);
-      const uint32_t tO = tbase + kColO;
       const uint32_t tQ = tbase + kColQ;
       // Descriptors are built once; per MMA only the start address moves
       // (the 14-bit address field never carries into the other fields).
       const uint64_t kdesc0 = sdesc_sw128(sStage, 16, 1024);
       const uint64_t qrdesc = sdesc_sw64(sQrope, 512);
       const uint64_t kropedesc0 = sdesc_sw64(sRope, 512);
-      const uint64_t vdesc0 = sdesc_sw128(sStage, kKAtomBytes, 1024);
       int g = 0, seg_i = 0;
       bool ok = true;
-      // S partial for global step gg: A = this CTA's q columns (TMEM), B = K atoms.
-      auto issue_s = [&](int gg) -> bool {
-        const uint32_t u = (uint32_t)gg;
-        const uint32_t slot = u & (kStages - 1);
-        if (!mbar_wait(bar_kv_full(slot), (u / kStages) & 1u, abort_flag, err, kSiteKvFull, gg))
-          return false;
-        tc_fence_after();
-        const uint64_t kd = kdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-        const uint32_t tS = tbase + kColS + (u & (kSBufs - 1)) * 64;
-        // c_kv atoms: q from TMEM; the RoPE half: q from shared memory
-        for (int a = 0; a < 4; ++a) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tS, tQ + a * 32 + kk * 8, kd + (uint64_t)((a * kKAtomBytes + kk * 32) >> 4),
-                   kIdescS, (a | kk) != 0);
-        }
-        {
-          const uint64_t rd = kropedesc0 + (uint64_t)((slot * kKropeBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kRopeCols / 16; ++kk)
-            mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
-                   kIdescS, 1u);
-        }
-        tc_commit(bar_s_full(u & (kSBufs - 1)));
-        return true;
-      };
-      // O[:, own columns] += P V for global step gg (P in TMEM over its S)
-      // O[:, own columns] += P V for global step gg.  pv_done is committed only
-      // after the PV of a segment's second-to-last step: the O rescale of any
-      // earlier step waits for the next step's S instead (issued after this
-      // PV, and a commit covers every earlier MMA of this thread).
-      auto issue_pv = [&](int gg, uint32_t acc_first, bool commit_done) -> bool {
-        const uint32_t u = (uint32_t)gg;
-        const uint32_t sb = u & (kSBufs - 1);
-        const uint32_t slot = u & (kStages - 1);
-        if (!mbar_wait(bar_p_full(sb), (u / kSBufs) & 1u, abort_flag, err, kSitePFull, gg))
-          return false;
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
-        const uint32_t aP = tbase + kColS + sb * 64;
-        mma_ts(tO, aP, vd, kIdescPV, acc_first);
-#pragma unroll
-        for (int kk = 1; kk < kStep / 16; ++kk)
-          mma_ts(tO, aP + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, 1u);
-        tc_commit(bar_kv_empty(slot));
-        if (commit_done) tc_commit(bar_pv_done);
-        return true;
-      };
       for (int k = cluster; k < nchunks && ok; k += nclusters) {
         ChunkIter it;
         it.init(prefix, bounds, cstart, B, k);
@@ -640,113 +626,153 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar_q_full, seg_i & 1, abort_flag, err, kSiteQFull, seg_i);
           if (!ok) break;
           tc_fence_after();
-          for (int i = 0; i < n && i < kSBufs && ok; ++i) ok = issue_s(g + i);
-          if (ok && n <= kSBufs) tc_commit(bar_q_free);  // every S of this segment issued
-          if (ok && seg_i > 0) {
-            ok = mbar_wait(bar_o_free, (seg_i - 1) & 1, abort_flag, err, kSitePvDone, seg_i);
-            tc_fence_after();
-          }
-          // step 0 (O starts from zero), then steady steps whose S two ahead
-          // is never the segment's last, then a tail of at most three steps
-          // that carries the hand-over commits: no branches in the steady
-          // part, where every instruction of this thread delays the pipe
-          if (ok) ok = issue_pv(g, 0u, n == 2);
-          if (ok && n > kSBufs) {
-            ok = issue_s(g + kSBufs);
-            if (ok && n == kSBufs + 1) tc_commit(bar_q_free);
-          }
-          int i = 1;
-          for (; i + kSBufs + 1 < n && ok; ++i) {
-            ok = issue_pv(g + i, 1u, false);
-            if (ok) ok = issue_s(g + i + kSBufs);
-          }
-          for (; i < n && ok; ++i) {
-            ok = issue_pv(g + i, 1u, i == n - 2);
-            if (ok && i + kSBufs < n) {
-              ok = issue_s(g + i + kSBufs);
-              if (ok && i + kSBufs == n - 1) tc_commit(bar_q_free);
+          for (int i = 0; i < n; ++i) {
+            const uint32_t u = (uint32_t)(g + i);
+            const uint32_t sb = u & (kSBufs - 1);
+            const uint32_t slot = u & (kStages - 1);
+            // every compute warp has read the buffer's previous S
+            if (u >= (uint32_t)kSBufs) {
+              ok = mbar_wait(bar_s_read(sb), ((u - kSBufs) / kSBufs) & 1u, abort_flag, err,
+                             kSiteXfree, (int)u);
+              if (!ok) break;
             }
+            ok = mbar_wait(bar_kv_full(slot), (u / kStages) & 1u, abort_flag, err, kSiteKvFull,
+                           (int)u);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kd = kdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
+            const uint32_t tS = tbase + kColS + sb * 64;
+            // c_kv atoms: q from TMEM; the RoPE half: q from shared memory
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tS, tQ + a * 32 + kk * 8,
+                       kd + (uint64_t)((a * kKAtomBytes + kk * 32) >> 4), kIdescS,
+                       (a | kk) != 0);
+            }
+            const uint64_t rd = kropedesc0 + (uint64_t)((slot * kKropeBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kRopeCols / 16; ++kk)
+              mma_ss(tS, qrdesc + (uint64_t)((kk * 32) >> 4), rd + (uint64_t)((kk * 32) >> 4),
+                     kIdescS, 1u);
+            tc_commit(bar_s_full(sb));
           }
-          if (ok) tc_commit(bar_o_ready);  // after the segment's last PV
+          if (!ok) break;
+          tc_commit(bar_q_free);  // every reader of this segment's q issued
           g += n;
           ++seg_i;
         }
       }
-      tc_commit(bar_mma_drain);
+      tc_commit(bar_drain_s);
       volatile int never = 0;
-      mbar_wait(bar_mma_drain, 0, &never, nullptr, kSiteDrain, -2);
+      mbar_wait(bar_drain_s, 0, &never, nullptr, kSiteDrain, -2);
     }
     __syncwarp();
-  } else if (warp >= 6) {
-    // ================= exchange warps (6-9): own partial S -> peer ===========
-    // Step k is sent (as two 32-token halves) once S(k) is in TMEM and this
-    // CTA's softmax warps have read the peer's step k-1: the peer cannot then
-    // reach a receive buffer that is still being read here.
-    const int r = (warp & 3) * 32 + lane;  // head == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS0 = tbase + lane_off + kColS;
-    const uint32_t peer_row = mapa_shared(sX + r * 16, peer);  // this head's 16 B of each quad
-    const uint32_t peer_xfull0 = mapa_shared(bar_xfull(0), peer);
-    int total = 0;
-    for (int k = cluster; k < nchunks; k += nclusters) {
-      ChunkIter it;
-      it.init(prefix, bounds, cstart, B, k);
-      Seg s;
-      while (it.next(s)) total += seg_steps(s.p0, s.p1, seqlens[s.b]);
-    }
-    for (int gg = 0; gg < total; ++gg) {
-      const int sb = gg % kSBufs;
-      bool w = mbar_wait(bar_s_full(sb), (gg / kSBufs) & 1, abort_flag, err, kSiteSFull, gg);
-      if (w && gg > 0) {
-        const int pb = (gg - 1) % kSBufs;
-        w = mbar_wait(bar_b_read(pb), ((gg - 1) / kSBufs) & 1, abort_flag, err, kSiteXfree, gg);
-      }
-      w = __all_sync(0xffffffffu, w);
-      if (!w) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float sv[kHalf];
-        tmem_ld32(tS0 + sb * 64 + h * 32, sv);
-        const int xb = (2 * gg + h) % kXBufs;
-        const uint32_t dst = peer_row + xb * kXBufBytes;
-        const uint32_t rbar = peer_xfull0 + 8u * xb;
+  } else if (warp == 10) {
+    // ================= PV issuer: O[:, own columns] += P V ==================
+    if (lane == 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16(kHq, 256, false, true);
+      const uint32_t tO = tbase + kColO;
+      const uint64_t pdesc0 = sdesc_sw64(sP, 512);
+      const uint64_t vdesc0 = sdesc_sw128(sStage, kKAtomBytes, 1024);
+      int g = 0, seg_i = 0;
+      bool ok = true;
+      for (int k = cluster; k < nchunks && ok; k += nclusters) {
+        ChunkIter it;
+        it.init(prefix, bounds, cstart, B, k);
+        Seg s;
+        while (ok && it.next(s)) {
+          const int n = seg_steps(s.p0, s.p1, seqlens[s.b]);
+          if (seg_i > 0) {  // the previous segment's epilogue has read O
+            ok = mbar_wait(bar_o_free, (seg_i - 1) & 1, abort_flag, err, kSitePvDone, seg_i);
+            if (!ok) break;
+          }
+          for (int i = 0; i < n; ++i) {
+            const uint32_t u = (uint32_t)(g + i);
+            const uint32_t pb = u & (kPSlots - 1);
+            const uint32_t slot = u & (kStages - 1);
+            ok = mbar_wait(bar_p_full(pb), (u / kPSlots) & 1u, abort_flag, err, kSitePFull,
+                           (int)u);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t pd = pdesc0 + (uint64_t)((pb * kPSlotBytes) >> 4);
+            const uint64_t vd = vdesc0 + (uint64_t)((slot * kStageBytes) >> 4);
 #pragma unroll
-        for (int c = 0; c < kHalf; c += 4)
-          st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
-                      __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
-                      __float_as_uint(sv[c + 3]), rbar);
+            for (int kk = 0; kk < kStep / 16; ++kk)
+              mma_ss(tO, pd + (uint64_t)(((kk >> 1) * kPAtomBytes + (kk & 1) * 32) >> 4),
+                     vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (i | kk) != 0);
+            tc_commit_mc(bar_kv_free(slot), 0x3);
+          }
+          if (!ok) break;
+          g += n;
+          ++seg_i;
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar_s_read(sb));
+      tc_commit(bar_drain_pv);
+      volatile int never = 0;
+      mbar_wait(bar_drain_pv, 0, &never, nullptr, kSiteDrain, -3);
     }
+    __syncwarp();
   } else {
-    // ================= softmax and epilogue (warps 0-3) ============
-    const int r = threadIdx.x;  // head == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tbase + lane_off + kColO;
+    // ================= compute warps 0-7 =================
+    // Warp w covers TMEM lanes (heads) 32 (w % 4) .. + 31.  Heads 64 rank ..
+    // + 63 are this CTA's own: their warps run the softmax, warp w for the
+    // tokens 32 (w / 4) .. + 31 of each step.  The other warps serve the
+    // peer's heads: they send this CTA's partial S of those heads (token half
+    // w / 4) and keep those heads' O rows (this CTA's columns) in step with
+    // the peer's softmax.  Every warp writes O columns 128 (w / 4) .. + 127
+    // of its rows in the epilogue.
+    const int sub = warp & 3, th = warp >> 2;
+    const bool own = (sub >> 1) == (int)rank;
+    const int h = sub * 32 + lane;       // head == TMEM lane
+    const int j = h & (kOwn - 1);        // its index among its owner's 64 heads
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const uint32_t tO = tbase + lane_off + kColO + th * 128;
     const uint32_t tQ = tbase + lane_off + kColQ;
-    const uint32_t tS0 = tbase + lane_off + kColS;
-    const uint8_t* my_row = smem + kXOff + r * 16;  // this head's 16 B of each token quad
+    const uint32_t tS = tbase + lane_off + kColS + th * kHalf;
+    const bool first_of_pair = (sub & 1) == 0;  // one warp per (role, half) arms barriers
+    float* lfin = reinterpret_cast<float*>(smem + kLfinOff);
+    const float* alpha_in = reinterpret_cast<const float*>(smem + kAlphaOff);
+    float* pmax = reinterpret_cast<float*>(smem + kPmaxOff);
+    float* lpart = reinterpret_cast<float*>(smem + kLpartOff);
+    const uint32_t peer_x = mapa_shared(sX + j * 16, peer);
+    const uint32_t peer_x_full0 = mapa_shared(bar_x_full(0), peer);
+    const uint32_t peer_alpha = mapa_shared(base + kAlphaOff + j * 4, peer);
+    const uint32_t peer_lfin = mapa_shared(base + kLfinOff + j * 4, peer);
+    const uint32_t peer_xp_full0 = mapa_shared(bar_xp_full(0), peer);
+    const uint32_t peer_lfin_full0 = mapa_shared(bar_lfin_full(0), peer);
+    const uint32_t peer_p = mapa_shared(sP, peer);
     constexpr float kLn2 = 0.69314718055994530942f;
     int g = 0, seg_i = 0;
-    int pvd = 0;  // pv_done phases completed before this segment
     bool ok = true;
     // the previous segment, whose epilogue runs once the next q is in place
-    int prev_b = -1, prev_slot = -1, prev_seg = 0;
+    int prev_b = -1, prev_slot = -1, prev_seg = 0, prev_last = 0;
     float prev_m = 0.f, prev_l = 0.f;
 
-    auto epilogue = [&]() {
-      // O / l -> bf16 (whole sequence) or fp32 partial; LSE from rank 0
-      const float inv_l = (prev_l > 0.f) ? 1.0f / prev_l : 0.f;
-      const float lse_v = (prev_l > 0.f) ? (prev_m + log2f(prev_l)) * kLn2 : -INFINITY;
-      const size_t orow = (size_t)prev_b * kHq + r;
+    // O / l of this warp's rows and columns -> bf16 (whole sequence) or an
+    // fp32 partial; the LSE of its own heads.  The peer's heads take the row
+    // sums the peer sent.
+    auto epilogue = [&]() -> bool {
+      float lv = prev_l;
+      if (!own) {
+        const int ls = prev_seg & 1;
+        const bool w = mbar_wait<true>(bar_lfin_full(ls), (prev_seg >> 1) & 1, abort_flag, err,
+                                       kSiteXchg, prev_seg);
+        if (!__all_sync(0xffffffffu, w)) return false;
+        lv = lfin[ls * kOwn + j];
+        if (first_of_pair && th == 0 && lane == 0)
+          mbar_arrive_expect_tx(bar_lfin_full(ls), kLfinBytes);  // for two segments on
+      }
+      const float inv_l = (lv > 0.f) ? 1.0f / lv : 0.f;
+      const size_t orow = (size_t)prev_b * kHq + h;
+      const int col0 = (int)rank * 256 + th * 128;
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = 0; c < 128; c += 32) {
         float ov[32];
         tmem_ld32(tO + c, ov);
         if (prev_slot < 0) {
-          __nv_bfloat16* dst = o + orow * kDv + rank * 256 + c;
+          __nv_bfloat16* dst = o + orow * kDv + col0 + c;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -757,7 +783,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
           }
         } else {
-          float* dst = part_o + ((size_t)prev_slot * kHq + r) * kDv + rank * 256 + c;
+          float* dst = part_o + ((size_t)prev_slot * kHq + h) * kDv + col0 + c;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
             *reinterpret_cast<float4*>(dst + q4 * 4) =
@@ -765,12 +791,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             ov[q4 * 4 + 3] * inv_l);
         }
       }
-      if (rank == 0) {
+      if (own && th == 0) {
+        const float lse_v = (lv > 0.f) ? (prev_m + log2f(lv)) * kLn2 : -INFINITY;
         if (prev_slot < 0) lse[orow] = lse_v;
-        else part_lse[(size_t)prev_slot * kHq + r] = lse_v;
+        else part_lse[(size_t)prev_slot * kHq + h] = lse_v;
       }
       tc_fence_before();
-      mbar_arrive(bar_o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_o_free);
+      return true;
     };
 
     for (int k = cluster; k < nchunks && ok; k += nclusters) {
@@ -781,248 +810,342 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int L = seqlens[s.b];
         const int t0 = s.p0 * kPage;
         const int n = seg_steps(s.p0, s.p1, L);
-        // ---- this segment's q columns -> TMEM (A operand of the S MMAs)
+        // ---- this segment's q: this warp's heads, c_kv atoms 2 th and 2 th + 1
+        //      -> TMEM (A operand of the S MMAs); the RoPE half -> shared memory
+        bool seg_ok = true;
         if (seg_i > 0) {
-          ok = mbar_wait(bar_q_free, (seg_i - 1) & 1, abort_flag, err, kSiteQFull, seg_i);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
+          seg_ok = __all_sync(0xffffffffu, mbar_wait(bar_q_free, (seg_i - 1) & 1, abort_flag,
+                                                     err, kSiteQFull, seg_i));
         }
-        {
-          const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + r) * kDk);
-          // all of this head's 256 columns in flight at once (one memory
-          // latency per segment, not one per atom), then into TMEM
-          uint4 qv[32];
+        if (seg_ok) {
+          const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + h) * kDk);
+          uint4 qv[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) qv[c] = __ldg(qrow + atom_col(0) / 8 + c);
+          for (int c = 0; c < 16; ++c) qv[c] = __ldg(qrow + atom_col(2 * th) / 8 + c);
+          uint4 rv[4];
+          if (th == 0) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
+            for (int c = 0; c < 4; ++c) rv[c] = __ldg(qrow + rope_col / 8 + c);
+          }
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint4 v = qv[a * 8 + c];
               w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
             }
-            tmem_st32(tQ + a * 32, w);
+            tmem_st32(tQ + (2 * th + a) * 32, w);
           }
-          {
-            // RoPE half -> shared memory, 64-byte rows with the 64-byte
-            // swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3))
-            uint8_t* qr = smem + kQropeOff + r * kRopeRowBytes;
+          if (th == 0) {
+            // 64-byte rows with the 64-byte swizzle: 16-byte chunk c of row r
+            // at chunk c ^ ((r >> 1) & 3)
+            uint8_t* qr = smem + kQropeOff + h * kRopeRowBytes;
 #pragma unroll
-            for (int c = 0; c < kRopeRowBytes / 16; ++c)
-              *reinterpret_cast<uint4*>(qr + ((c ^ ((r >> 1) & 3)) * 16)) =
-                  __ldg(qrow + rope_col / 8 + c);
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(qr + ((c ^ ((h >> 1) & 3)) * 16)) = rv[c];
             fence_proxy_async_smem();
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(bar_q_full);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_q_full);
         }
         // ---- the previous segment's epilogue overlaps this segment's first S
-        if (prev_b >= 0) {
-          ok = mbar_wait(bar_o_ready, prev_seg & 1, abort_flag, err, kSitePvDone, prev_seg);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-          epilogue();
-          prev_b = -1;
+        if (seg_ok && prev_b >= 0) {
+          seg_ok = __all_sync(0xffffffffu,
+                              mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)),
+                                              (prev_last / kStages) & 1, abort_flag, err,
+                                              kSitePvDone, prev_seg));
+          if (seg_ok) {
+            tc_fence_after();
+            seg_ok = epilogue();
+            prev_b = -1;
+          }
         }
-        float m_ref = -INFINITY, l = 0.f;
-        for (int i = 0; i < n && ok; ++i) {
-          const int gi = g + i;
-          const int sb = gi % kSBufs;
-          const int nvalid = L - (t0 + i * kStep);
-          const bool full = nvalid >= kStep;
-          // waits for the peer's half h and for this CTA's own partial
-          auto wait_peer = [&](int h) -> bool {
-            const int xb = (2 * gi + h) % kXBufs;
-            const bool w = mbar_wait<true>(bar_xfull(xb), ((2 * gi + h) / kXBufs) & 1,
-                                           abort_flag, err, kSiteXchg, gi);
-            return __all_sync(0xffffffffu, w);
-          };
-          bool s_seen = false;
-          auto wait_own = [&]() -> bool {
-            if (s_seen) return true;
-            const bool w = __all_sync(0xffffffffu, mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1,
-                                                             abort_flag, err, kSiteSFull, gi));
-            if (w) tc_fence_after();
-            s_seen = w;
-            return w;
-          };
-          uint32_t p[kStep / 2];
-          float alpha = 1.f;
-          bool resc = false;
-          bool done = false;
-          // Fast path (whole page visible, reference set, scale >= 0): each
-          // 32-token half is summed (own + peer partial: one rounding, the
-          // same bits on both CTAs) and turned into P = 2^(scale*s - m_ref)
-          // with the CURRENT reference as soon as it has arrived; kept while
-          // every row sum is at most 2^16 (which bounds every P).  Otherwise
-          // the slow path below redoes the step from the exact row max.
-          if (__all_sync(0xffffffffu, full && m_ref != -INFINITY && scale_log2 >= 0.f)) {
-            float rr[8];
+        // the softmax warps leave together: their named barrier has no time limit
+        if (own) seg_ok = !named_barrier_any(1, 128, !seg_ok);
+        if (!seg_ok) {
+          ok = false;
+          break;
+        }
+        if (own) {
+          // ================= softmax of this CTA's heads =================
+          // The four softmax warps agree on every fast/slow and failure
+          // decision through named barrier 1 (a barrier has no time limit, so
+          // a failed wait is carried to the next barrier, never out of the
+          // loop on its own).
+          float m_ref = -INFINITY, l = 0.f;  // l: this thread's token half
+          bool failed = false;
+          const int st = th * 64 + (sub & 1) * 32 + lane;  // 0..127 over the softmax warps
+          for (int i = 0; i < n; ++i) {
+            const int gi = g + i;
+            const int sb = gi & (kSBufs - 1);
+            const int xs = (gi & 1) * 2 + th;
+            const int nvalid = L - (t0 + i * kStep);
+            const int nv = nvalid - th * kHalf;  // valid tokens of this half
+            float t[kHalf];
+            if (!failed) {
+              const bool w = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err,
+                                       kSiteSFull, gi);
+              failed = !__all_sync(0xffffffffu, w);
+            }
+            if (!failed) {
+              tc_fence_after();
+              tmem_ld32(tS + sb * 64, t);
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_s_read(sb));
+              const bool w = mbar_wait<true>(bar_x_full(xs), (gi >> 1) & 1, abort_flag, err,
+                                             kSiteXchg, gi);
+              failed = !__all_sync(0xffffffffu, w);
+            }
+            if (!failed) {
+              // the score: this CTA's partial plus the peer's partial
+              const uint8_t* xin = smem + kXOff + xs * kXMsgBytes + j * 16;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
-            const float nm = -m_ref;
+              for (int c = 0; c < kHalf; c += 4) {
+                const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
+                t[c] += pv.x; t[c + 1] += pv.y; t[c + 2] += pv.z; t[c + 3] += pv.w;
+              }
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(bar_x_read(xs));
+                if (first_of_pair) mbar_arrive_expect_tx(bar_x_full(xs), kXMsgBytes);
+              }
+            }
+            uint32_t p[kHalf / 2];
+            float alpha = 1.f;
+            bool resc = false;
+            // Fast path (whole page visible, reference set, scale >= 0): P =
+            // 2^(scale*s - m_ref) with the current reference, kept while every
+            // thread's half-row sum is at most 2^16 (which bounds every P).
+            bool fast = !failed && __all_sync(0xffffffffu, nvalid >= kStep && m_ref != -INFINITY &&
+                                                              scale_log2 >= 0.f);
+            float rs = 0.f;
+            if (fast) {
+              float rr[8];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              ok = wait_peer(h) && wait_own();
-              if (!ok) break;
-              float sh[kHalf];
-              tmem_ld32(tS0 + sb * 64 + h * 32, sh);
-              const uint8_t* xin = my_row + ((2 * gi + h) % kXBufs) * kXBufBytes;
+              for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+              const float nm = -m_ref;
 #pragma unroll
               for (int c = 0; c < kHalf; c += 8) {
-                const float4 qa = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
-                const float4 qb = *reinterpret_cast<const float4*>(xin + (c / 4 + 1) * kXQuadBytes);
-                const float pxv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
                 float tv[8], pv[8];
 #pragma unroll
-                for (int u = 0; u < 8; u += 2) {
-                  float s0, s1;
-                  ffma2(s0, s1, sh[c + u], sh[c + u + 1], 1.f, 1.f, pxv[u], pxv[u + 1]);
-                  ffma2(tv[u], tv[u + 1], s0, s1, scale_log2, scale_log2, nm, nm);
-                }
+                for (int u = 0; u < 8; u += 2)
+                  ffma2(tv[u], tv[u + 1], t[c + u], t[c + u + 1], scale_log2, scale_log2, nm, nm);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
 #pragma unroll
                 for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
 #pragma unroll
-                for (int u = 0; u < 8; u += 2)
-                  p[(h * kHalf + c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+                for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
               }
+              rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+              fast = rs <= 65536.f;
             }
-            if (!ok) break;
-            const float rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
-            if (__all_sync(0xffffffffu, rs <= 65536.f)) {
-              l += rs;
-              done = true;
-            }
-          }
-          if (!done) {
-            // slow path: the whole step (masked) from its exact row max
-            ok = wait_peer(0) && wait_peer(1) && wait_own();
-            if (!ok) break;
-            float px[kStep];
+            if (named_barrier_any(1, 128, failed || !fast)) {
+              // slow path (or a failure somewhere): the step from its exact
+              // row max over both token halves
+              float mx = -INFINITY;
+              if (!failed) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint8_t* xin = my_row + ((2 * gi + h) % kXBufs) * kXBufBytes;
+                for (int c = 0; c < kHalf; ++c) {
+                  t[c] = (c < nv) ? t[c] * scale_log2 : -INFINITY;
+                  mx = fmaxf(mx, t[c]);
+                }
+                pmax[((gi & 1) * 2 + th) * kOwn + j] = mx;
+              }
+              if (named_barrier_any(1, 128, failed)) {
+                ok = false;
+                break;
+              }
+              const float mt = fmaxf(mx, pmax[((gi & 1) * 2 + (th ^ 1)) * kOwn + j]);
+              const float m_new = fmaxf(m_ref, mt);
+              resc = m_new > m_ref + kRescaleThreshold;
+              if (resc) {
+                alpha = fast_exp2(m_ref - m_new);
+                m_ref = m_new;
+                l *= alpha;
+              }
+              const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+              float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
               for (int c = 0; c < kHalf; c += 4) {
-                const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
-                px[h * 32 + c] = pv.x; px[h * 32 + c + 1] = pv.y;
-                px[h * 32 + c + 2] = pv.z; px[h * 32 + c + 3] = pv.w;
+                const float p0 = fast_exp2(t[c] - m_use);
+                const float p1 = fast_exp2(t[c + 1] - m_use);
+                const float p2 = fast_exp2(t[c + 2] - m_use);
+                const float p3 = fast_exp2(t[c + 3] - m_use);
+                rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
+                p[c / 2] = pack_bf16x2(p0, p1);
+                p[c / 2 + 1] = pack_bf16x2(p2, p3);
               }
-            }
-            float sv[kStep];
-            tmem_ld64(tS0 + sb * 64, sv);
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kStep; c += 4) {
-              float t4[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float sum = sv[c + u] + px[c + u];
-                t4[u] = (c + u < nvalid) ? sum * scale_log2 : -INFINITY;
-                sv[c + u] = t4[u];
-              }
-              mx0 = fmaxf(mx0, t4[0]); mx1 = fmaxf(mx1, t4[1]);
-              mx2 = fmaxf(mx2, t4[2]); mx3 = fmaxf(mx3, t4[3]);
-            }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            const float m_new = fmaxf(m_ref, mt);
-            resc = m_new > m_ref + kRescaleThreshold;
-            if (resc) {
-              alpha = fast_exp2(m_ref - m_new);
-              m_ref = m_new;
-              l *= alpha;
-            }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < kStep; c += 4) {
-              const float p0 = fast_exp2(sv[c] - m_use);
-              const float p1 = fast_exp2(sv[c + 1] - m_use);
-              const float p2 = fast_exp2(sv[c + 2] - m_use);
-              const float p3 = fast_exp2(sv[c + 3] - m_use);
-              rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
-              p[c / 2] = pack_bf16x2(p0, p1);
-              p[c / 2 + 1] = pack_bf16x2(p2, p3);
-            }
-            l += (rs0 + rs1) + (rs2 + rs3);
-          }
-          // Every read of the peer's partial of this step has returned: re-arm
-          // both half-buffers for step gi + 2 (the peer sends that step only
-          // after this CTA has sent step gi + 1, which waits for every thread's
-          // b_read of this step), then release them.
-          if (r == 0) {
-            mbar_arrive_expect_tx(bar_xfull((2 * gi) % kXBufs), kXBytes);
-            mbar_arrive_expect_tx(bar_xfull((2 * gi + 1) % kXBufs), kXBytes);
-          }
-          mbar_arrive(bar_b_read(sb));
-          // Tokens past the end contribute exactly zero even if the cache
-          // tail holds non-finite bytes: clear those V rows before PV reads.
-          // Each thread fences its own writes; the PV MMA is issued only after
-          // all 128 threads have arrived on p_full below.
-          if (nvalid < kStep) {
-            uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
-            const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
-            for (int e = threadIdx.x; e < zrows * 4 * 8; e += 128) {
-              const int a = e / (zrows * 8), rem = e % (zrows * 8);
-              const int rr = nvalid + rem / 8, ch = rem % 8;
-              *reinterpret_cast<uint4*>(vst + a * kKAtomBytes + rr * 128 + ch * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-          }
-          // O is rescaled once the previous step's PV is done: seen through
-          // the next step's S (issued after that PV), or, at a segment's last
-          // step, through pv_done (committed once per segment of two or more
-          // steps, after the PV of its second-to-last step).
-          if (i > 0 && __any_sync(0xffffffffu, resc)) {
-            if (i + 1 < n) {
-              const int gn = gi + 1;
-              ok = mbar_wait(bar_s_full(gn % kSBufs), (gn / kSBufs) & 1, abort_flag, err,
-                             kSitePvDone, gi);
+              l += (rs0 + rs1) + (rs2 + rs3);
             } else {
-              ok = mbar_wait(bar_pv_done, pvd & 1, abort_flag, err, kSitePvDone, gi);
+              l += rs;
             }
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
+            // O rows of these heads (this warp's columns): rescaled once the
+            // previous step's PV is done on this CTA
+            if (!failed && i > 0 && __any_sync(0xffffffffu, resc)) {
+              const int gp = gi - 1;
+              const bool w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
+                                             abort_flag, err, kSitePvDone, gi);
+              failed = !__all_sync(0xffffffffu, w);
+              if (!failed) {
+                tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 256; c += 32) {
-              float ov[32];
-              tmem_ld32(tO + c, ov);
-              uint32_t ou[32];
+                for (int c = 0; c < 128; c += 32) {
+                  float ov[32];
+                  tmem_ld32(tO + c, ov);
+                  uint32_t ou[32];
 #pragma unroll
-              for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
-              tmem_st32(tO + c, ou);
+                  for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
+                  tmem_st32(tO + c, ou);
+                }
+                tmem_st_wait();
+              }
+            }
+            // the step's P slot is free once both CTAs' PV of step gi - 2 is done
+            if (!failed && gi >= kPSlots) {
+              const int gp = gi - kPSlots;
+              const bool w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
+                                             abort_flag, err, kSiteXfree, gi);
+              failed = !__all_sync(0xffffffffu, w);
+            }
+            if (!failed) {
+              const int patom = (gi & 1) * kPSlotBytes + th * kPAtomBytes;
+              uint8_t* prow = smem + kPOff + patom + h * 64;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) =
+                    make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+              // the peer scales its O rows of these heads by the same factor
+              if (th == 0)
+                st_async_b32(peer_alpha + (gi & 1) * kOwn * 4, __float_as_uint(alpha),
+                             peer_xp_full0 + 8u * (gi & 1));
+              // Tokens past the end contribute exactly zero even if the cache
+              // tail holds non-finite bytes: clear those V rows of this CTA's
+              // stage before its PV reads them (p_full waits for all four
+              // softmax warps).
+              if (nvalid < kStep) {
+                uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
+                const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
+                for (int e = st; e < zrows * 4 * 8; e += 128) {
+                  const int a = e / (zrows * 8), rem = e % (zrows * 8);
+                  const int rr = nvalid + rem / 8, ch = rem % 8;
+                  *reinterpret_cast<uint4*>(vst + a * kKAtomBytes + rr * 128 + ch * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+                }
+              }
+              fence_proxy_async_smem();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                const int off = patom + sub * 32 * 64;  // this warp's 32 rows of the atom
+                bulk_copy_to_peer(peer_p + off, sP + off, kPWarpBytes,
+                                  peer_xp_full0 + 8u * (gi & 1));
+                mbar_arrive(bar_p_full(gi & 1));
+              }
             }
           }
-          // P overwrites the S buffer: the exchange warps must have read it
-          ok = mbar_wait(bar_s_read(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull, gi);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-          tmem_st32(tS0 + sb * 64, p);
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar_p_full(sb));
+          if (ok) {
+            // the row sums over both token halves; the peer gets them for its
+            // O rows of these heads
+            lpart[th * kOwn + j] = l;
+            if (named_barrier_any(1, 128, failed)) {
+              ok = false;
+            } else {
+              const float lt = lpart[j] + lpart[kOwn + j];
+              if (th == 0)
+                st_async_b32(peer_lfin + (seg_i & 1) * kOwn * 4, __float_as_uint(lt),
+                             peer_lfin_full0 + 8u * (seg_i & 1));
+              prev_m = m_ref;
+              prev_l = lt;
+            }
+          }
+        } else {
+          // ================= the peer's heads =================
+          // Iteration i sends this CTA's partial S of step i (token half th)
+          // to the peer, then takes in the peer's P rows of step i - 1: their
+          // rescale factors are applied to this CTA's O rows of those heads
+          // before the PV of that step may run.
+          for (int i = 0; i <= n && ok; ++i) {
+            if (i < n) {
+              const int gi = g + i;
+              const int sb = gi & (kSBufs - 1);
+              const int xs = (gi & 1) * 2 + th;
+              bool w = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull,
+                                 gi);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+              tc_fence_after();
+              float sv[kHalf];
+              tmem_ld32(tS + sb * 64, sv);
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_s_read(sb));
+              // The peer sends its step gi + 1 into the slot of step gi - 1 only
+              // after its softmax has read this CTA's step gi, which is sent
+              // only after this CTA's softmax has read the peer's step gi - 1.
+              if (gi >= 1) {
+                const int gp = gi - 1;
+                w = mbar_wait(bar_x_read((gp & 1) * 2 + th), (gp >> 1) & 1, abort_flag, err,
+                              kSiteXfree, gi);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+              }
+              const uint32_t dst = peer_x + xs * kXMsgBytes;
+              const uint32_t rbar = peer_x_full0 + 8u * xs;
+#pragma unroll
+              for (int c = 0; c < kHalf; c += 4)
+                st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
+                            __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
+                            __float_as_uint(sv[c + 3]), rbar);
+            }
+            if (i > 0) {
+              const int gp = g + i - 1;
+              const int pb = gp & (kPSlots - 1);
+              bool w = mbar_wait<true>(bar_xp_full(pb), (gp >> 1) & 1, abort_flag, err,
+                                       kSitePFull, gp);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+              if (first_of_pair && th == 0 && lane == 0)
+                mbar_arrive_expect_tx(bar_xp_full(pb), kXpBytes);  // for step gp + 2
+              if (i > 1) {
+                const float a = alpha_in[pb * kOwn + j];
+                if (__any_sync(0xffffffffu, a != 1.f)) {
+                  const int gq = gp - 1;
+                  w = mbar_wait<true>(bar_kv_free(gq & (kStages - 1)), (gq / kStages) & 1,
+                                      abort_flag, err, kSitePvDone, gp);
+                  if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                  tc_fence_after();
+#pragma unroll 1
+                  for (int c = 0; c < 128; c += 32) {
+                    float ov[32];
+                    tmem_ld32(tO + c, ov);
+                    uint32_t ou[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * a);
+                    tmem_st32(tO + c, ou);
+                  }
+                  tmem_st_wait();
+                }
+              }
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_p_full(pb));
+            }
+          }
         }
         if (!ok) break;
         prev_b = s.b;
         prev_slot = s.slot;
         prev_seg = seg_i;
-        prev_m = m_ref;
-        prev_l = l;
-        if (n >= 2) ++pvd;
+        prev_last = g + n - 1;
         g += n;
         ++seg_i;
       }
     }
     if (ok && prev_b >= 0) {
-      ok = mbar_wait(bar_o_ready, prev_seg & 1, abort_flag, err, kSitePvDone, prev_seg);
+      ok = mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)), (prev_last / kStages) & 1,
+                           abort_flag, err, kSitePvDone, prev_seg);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
@@ -1033,18 +1156,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  // After an abort the peer may have left its loops with a partial-score
-  // store to this CTA still in flight, one that this CTA's softmax never
-  // waited for (a store lands in well under a microsecond).  A CTA that
-  // aborted waits 50 us before it arrives at the cluster barrier below, so
-  // the peer cannot leave while one of this CTA's own stores is in flight.
+  // After an abort the peer may have left its loops with a store or copy to
+  // this CTA still in flight, one that this CTA never waited for (they land in
+  // well under a microsecond).  A CTA that aborted waits 50 us before it
+  // arrives at the cluster barrier below, so the peer cannot leave while one
+  // of this CTA's own stores or copies is in flight.
   if (*abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 50000ull) {
     }
   }
   cluster_sync();  // no CTA leaves while its peer may still touch its smem
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }

@@ -173,6 +173,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
       : "memory");
 }
 
+// Asynchronous 4-byte store into a peer CTA's shared memory, counted (4 bytes)
+// on the peer's mbarrier `remote_bar` (shared::cluster addresses).
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v,
+                                             uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          remote_addr),
+      "r"(v), "r"(remote_bar)
+      : "memory");
+}
+
 // --------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -306,6 +317,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           bar)
+      : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in every CTA of the cluster named
+// by `cta_mask` when every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
