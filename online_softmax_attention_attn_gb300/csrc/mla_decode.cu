@@ -53,11 +53,10 @@ constexpr int kDk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
 constexpr int kStep = 64;                 // tokens per MMA step (one page)
-constexpr int kHalf = 32;                 // tokens per softmax warp and per partial-S message
 constexpr int kOwn = kHq / 2;             // heads whose softmax runs on each CTA
-// Warps 0-7 compute (warp w: TMEM lane quarter w % 4, token half / column
-// half w / 4; the softmax for this CTA's 64 heads, or the partial-S sends and
-// O upkeep for the peer's 64), 8 TMA producer, 9 S-MMA issuer, 10 PV-MMA issuer.
+// Warps 0-7 compute (warp w: TMEM lane quarter w % 4, the steps of parity
+// w / 4; the softmax for this CTA's 64 heads, or the partial-S sends and O
+// upkeep for the peer's 64), 8 TMA producer, 9 S-MMA issuer, 10 PV-MMA issuer.
 constexpr int kThreads = 352;
 constexpr int kKAtomBytes = kStep * 128;  // 64 tokens x 64 bf16
 constexpr int kStageBytes = 4 * kKAtomBytes;  // the CTA's 4 c_kv atoms (K and V): 32 KB
@@ -74,14 +73,14 @@ constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 static_assert((kStages & (kStages - 1)) == 0 && (kSBufs & (kSBufs - 1)) == 0 &&
                   (kRopeSlots & (kRopeSlots - 1)) == 0,
               "ring positions are taken with masks");
-// A partial-S message: one token half of one step for the 64 heads of the
-// receiving CTA, [token quad][head][4 tokens] fp32: 16 B per head and quad, so
+// A partial-S message: one step for the 64 heads of the receiving CTA,
+// [token quad][head][4 tokens] fp32: 16 B per head and quad, so
 // one warp store covers 512 contiguous bytes (contiguous remote stores move
 // about twice the bytes per clock of row-scattered ones) and each head's
 // reads are conflict-free.
 constexpr int kXQuadBytes = kOwn * 16;                 // 1 KB
-constexpr int kXMsgBytes = (kHalf / 4) * kXQuadBytes;  // 8 KB
-constexpr int kXSlots = 2 * 2;                         // two steps x two token halves
+constexpr int kXMsgBytes = (kStep / 4) * kXQuadBytes;  // 16 KB
+constexpr int kXSlots = 2;                             // two steps
 // P of one step in shared memory (the A operand of the PV MMAs): two K-major
 // atoms of 32 tokens (64-byte rows, 64-byte swizzle) over the 128 head rows.
 // A warp's 32 rows of one atom are 2 KB contiguous, which is what it copies
@@ -105,12 +104,13 @@ constexpr int kPOff = kXOff + kXSlots * kXMsgBytes;
 static_assert(kPOff % 1024 == 0, "P atoms start on swizzle-pattern boundaries");
 constexpr int kAlphaOff = kPOff + kPSlots * kPSlotBytes;  // [P slot][64] factors from the peer
 constexpr int kLfinOff = kAlphaOff + kPSlots * kOwn * 4;   // [segment parity][64] from the peer
-constexpr int kPmaxOff = kLfinOff + 2 * kOwn * 4;          // [step parity][half][64] row maxima
-constexpr int kLpartOff = kPmaxOff + 2 * 2 * kOwn * 4;     // [half][64] row sums
-constexpr int kBarOff = kLpartOff + 2 * kOwn * 4;
-// barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[4], x_read[4],
-// p_full[2], xp_full[2], lfin_full[2], q_full, q_free, o_free, drain_s, drain_pv
-constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 2 * kXSlots + 3 * kPSlots + 5;
+constexpr int kMpubOff = kLfinOff + 2 * kOwn * 4;          // [step parity][64] running maxima
+constexpr int kLpartOff = kMpubOff + 2 * kOwn * 4;         // [segment parity][step parity][l | m]
+constexpr int kBarOff = kLpartOff + 2 * 2 * kOwn * 8;
+// barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[2], x_read[2],
+// p_full[2], xp_full[2], lfin_full[2], m_ready[2], q_full, q_free, o_free,
+// seg_done, drain_s, drain_pv
+constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 2 * kXSlots + 4 * kPSlots + 6;
 constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -488,12 +488,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar_p_full = [&](int b) { return bar0 + 8u * (kBarP + b); };
   auto bar_xp_full = [&](int b) { return bar0 + 8u * (kBarP + kPSlots + b); };
   auto bar_lfin_full = [&](int b) { return bar0 + 8u * (kBarP + 2 * kPSlots + b); };
-  const uint32_t bar_q_full = bar0 + 8u * (kBarP + 3 * kPSlots);
+  // m_ready(b): the softmax warps of a step of parity b have published the
+  // running max after it (the next step's warps need it)
+  auto bar_m_ready = [&](int b) { return bar0 + 8u * (kBarP + 3 * kPSlots + b); };
+  const uint32_t bar_q_full = bar0 + 8u * (kBarP + 4 * kPSlots);
   const uint32_t bar_q_free = bar_q_full + 8;
   const uint32_t bar_o_free = bar_q_full + 16;
-  const uint32_t bar_drain_s = bar_q_full + 24;
-  const uint32_t bar_drain_pv = bar_q_full + 32;
-  static_assert(kBarP + 3 * kPSlots + 5 == kNumBars, "barrier count");
+  const uint32_t bar_seg_done = bar_q_full + 24;
+  const uint32_t bar_drain_s = bar_q_full + 32;
+  const uint32_t bar_drain_pv = bar_q_full + 40;
+  static_assert(kBarP + 4 * kPSlots + 6 == kNumBars, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -506,20 +510,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar_s_full(b), 1);
-      mbar_init(bar_s_read(b), 8);  // every compute warp reads every S
+      mbar_init(bar_s_read(b), 4);  // the four compute warps of the step's parity
     }
     for (int x = 0; x < kXSlots; ++x) {
       mbar_init(bar_x_full(x), 1);
-      mbar_init(bar_x_read(x), 2);  // the two softmax warps of the half
+      mbar_init(bar_x_read(x), 2);  // the two softmax warps of the step's parity
     }
     for (int b = 0; b < kPSlots; ++b) {
-      mbar_init(bar_p_full(b), 8);
+      mbar_init(bar_p_full(b), 4);
       mbar_init(bar_xp_full(b), 1);
       mbar_init(bar_lfin_full(b), 1);
+      mbar_init(bar_m_ready(b), 2);
     }
     mbar_init(bar_q_full, 8);
     mbar_init(bar_q_free, 1);
     mbar_init(bar_o_free, 8);
+    mbar_init(bar_seg_done, 4);  // the four softmax warps
     mbar_init(bar_drain_s, 1);
     mbar_init(bar_drain_pv, 1);
     *abort_flag = 0;
@@ -716,25 +722,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================= compute warps 0-7 =================
-    // Warp w covers TMEM lanes (heads) 32 (w % 4) .. + 31.  Heads 64 rank ..
-    // + 63 are this CTA's own: their warps run the softmax, warp w for the
-    // tokens 32 (w / 4) .. + 31 of each step.  The other warps serve the
-    // peer's heads: they send this CTA's partial S of those heads (token half
-    // w / 4) and keep those heads' O rows (this CTA's columns) in step with
-    // the peer's softmax.  Every warp writes O columns 128 (w / 4) .. + 127
-    // of its rows in the epilogue.
-    const int sub = warp & 3, th = warp >> 2;
+    // Warp w covers TMEM lanes (heads) 32 (w % 4) .. + 31 and the steps of
+    // parity w / 4.  Heads 64 rank .. + 63 are this CTA's own: their warps run
+    // the softmax of whole 64-token rows, the two parities in ping-pong (a warp
+    // has two steps' time for one, so one warp's waits overlap the other's
+    // work).  The other warps serve the peer's heads: they send this CTA's
+    // partial S of those heads and keep those heads' O rows (this CTA's
+    // columns) in step with the peer's softmax.  In the epilogue warp w writes
+    // O columns 128 (w / 4) .. + 127 of its rows.
+    const int sub = warp & 3, par = warp >> 2;
     const bool own = (sub >> 1) == (int)rank;
     const int h = sub * 32 + lane;       // head == TMEM lane
     const int j = h & (kOwn - 1);        // its index among its owner's 64 heads
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-    const uint32_t tO = tbase + lane_off + kColO + th * 128;
+    const uint32_t tO = tbase + lane_off + kColO;
     const uint32_t tQ = tbase + lane_off + kColQ;
-    const uint32_t tS = tbase + lane_off + kColS + th * kHalf;
-    const bool first_of_pair = (sub & 1) == 0;  // one warp per (role, half) arms barriers
-    float* lfin = reinterpret_cast<float*>(smem + kLfinOff);
+    const uint32_t tS = tbase + lane_off + kColS;
+    const bool first_of_pair = (sub & 1) == 0;  // one warp per (role, parity) arms barriers
+    const float* lfin = reinterpret_cast<const float*>(smem + kLfinOff);
     const float* alpha_in = reinterpret_cast<const float*>(smem + kAlphaOff);
-    float* pmax = reinterpret_cast<float*>(smem + kPmaxOff);
+    float* mpub = reinterpret_cast<float*>(smem + kMpubOff);
     float* lpart = reinterpret_cast<float*>(smem + kLpartOff);
     const uint32_t peer_x = mapa_shared(sX + j * 16, peer);
     const uint32_t peer_x_full0 = mapa_shared(bar_x_full(0), peer);
@@ -750,6 +757,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int prev_b = -1, prev_slot = -1, prev_seg = 0, prev_last = 0;
     float prev_m = 0.f, prev_l = 0.f;
 
+    // this warp's rows of O (all 256 of this CTA's columns) times a
+    auto rescale_o = [&](float a) {
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 32) {
+        float ov[32];
+        tmem_ld32(tO + c, ov);
+        uint32_t ou[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * a);
+        tmem_st32(tO + c, ou);
+      }
+      tmem_st_wait();
+    };
+
     // O / l of this warp's rows and columns -> bf16 (whole sequence) or an
     // fp32 partial; the LSE of its own heads.  The peer's heads take the row
     // sums the peer sent.
@@ -761,16 +782,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                        kSiteXchg, prev_seg);
         if (!__all_sync(0xffffffffu, w)) return false;
         lv = lfin[ls * kOwn + j];
-        if (first_of_pair && th == 0 && lane == 0)
+        if (first_of_pair && par == 0 && lane == 0)
           mbar_arrive_expect_tx(bar_lfin_full(ls), kLfinBytes);  // for two segments on
       }
       const float inv_l = (lv > 0.f) ? 1.0f / lv : 0.f;
       const size_t orow = (size_t)prev_b * kHq + h;
-      const int col0 = (int)rank * 256 + th * 128;
+      const int col0 = (int)rank * 256 + par * 128;
 #pragma unroll 1
       for (int c = 0; c < 128; c += 32) {
         float ov[32];
-        tmem_ld32(tO + c, ov);
+        tmem_ld32(tO + par * 128 + c, ov);
         if (prev_slot < 0) {
           __nv_bfloat16* dst = o + orow * kDv + col0 + c;
 #pragma unroll
@@ -791,7 +812,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             ov[q4 * 4 + 3] * inv_l);
         }
       }
-      if (own && th == 0) {
+      if (own && par == 0) {
         const float lse_v = (lv > 0.f) ? (prev_m + log2f(lv)) * kLn2 : -INFINITY;
         if (prev_slot < 0) lse[orow] = lse_v;
         else part_lse[(size_t)prev_slot * kHq + h] = lse_v;
@@ -810,20 +831,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int L = seqlens[s.b];
         const int t0 = s.p0 * kPage;
         const int n = seg_steps(s.p0, s.p1, L);
-        // ---- this segment's q: this warp's heads, c_kv atoms 2 th and 2 th + 1
-        //      -> TMEM (A operand of the S MMAs); the RoPE half -> shared memory
-        bool seg_ok = true;
+        // ---- this segment's q: this warp's heads, c_kv atoms 2 par and
+        //      2 par + 1 -> TMEM (A operand of the S MMAs); the RoPE half ->
+        //      shared memory
         if (seg_i > 0) {
-          seg_ok = __all_sync(0xffffffffu, mbar_wait(bar_q_free, (seg_i - 1) & 1, abort_flag,
-                                                     err, kSiteQFull, seg_i));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_q_free, (seg_i - 1) & 1, abort_flag, err,
+                                                 kSiteQFull, seg_i));
+          if (!ok) break;
         }
-        if (seg_ok) {
+        {
           const uint4* qrow = reinterpret_cast<const uint4*>(q + ((size_t)s.b * kHq + h) * kDk);
           uint4 qv[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) qv[c] = __ldg(qrow + atom_col(2 * th) / 8 + c);
+          for (int c = 0; c < 16; ++c) qv[c] = __ldg(qrow + atom_col(2 * par) / 8 + c);
           uint4 rv[4];
-          if (th == 0) {
+          if (par == 0) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) rv[c] = __ldg(qrow + rope_col / 8 + c);
           }
@@ -835,9 +857,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint4 v = qv[a * 8 + c];
               w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
             }
-            tmem_st32(tQ + (2 * th + a) * 32, w);
+            tmem_st32(tQ + (2 * par + a) * 32, w);
           }
-          if (th == 0) {
+          if (par == 0) {
             // 64-byte rows with the 64-byte swizzle: 16-byte chunk c of row r
             // at chunk c ^ ((r >> 1) & 3)
             uint8_t* qr = smem + kQropeOff + h * kRopeRowBytes;
@@ -852,286 +874,245 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar_q_full);
         }
         // ---- the previous segment's epilogue overlaps this segment's first S
-        if (seg_ok && prev_b >= 0) {
-          seg_ok = __all_sync(0xffffffffu,
-                              mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)),
-                                              (prev_last / kStages) & 1, abort_flag, err,
-                                              kSitePvDone, prev_seg));
-          if (seg_ok) {
-            tc_fence_after();
-            seg_ok = epilogue();
-            prev_b = -1;
-          }
-        }
-        // the softmax warps leave together: their named barrier has no time limit
-        if (own) seg_ok = !named_barrier_any(1, 128, !seg_ok);
-        if (!seg_ok) {
-          ok = false;
-          break;
+        if (prev_b >= 0) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)),
+                                          (prev_last / kStages) & 1, abort_flag, err,
+                                          kSitePvDone, prev_seg));
+          if (!ok) break;
+          tc_fence_after();
+          ok = epilogue();
+          if (!ok) break;
+          prev_b = -1;
         }
         if (own) {
           // ================= softmax of this CTA's heads =================
-          // The four softmax warps agree on every fast/slow and failure
-          // decision through named barrier 1 (a barrier has no time limit, so
-          // a failed wait is carried to the next barrier, never out of the
-          // loop on its own).
-          float m_ref = -INFINITY, l = 0.f;  // l: this thread's token half
-          bool failed = false;
-          const int st = th * 64 + (sub & 1) * 32 + lane;  // 0..127 over the softmax warps
-          for (int i = 0; i < n; ++i) {
+          float m_known = -INFINITY;  // the running max this warp's l is relative to
+          float l = 0.f;              // this warp's share of the row sum
+          for (int i = (par - g) & 1; i < n; i += 2) {
             const int gi = g + i;
-            const int sb = gi & (kSBufs - 1);
-            const int xs = (gi & 1) * 2 + th;
+            const int b = gi & 1;  // S buffer, message slots and P slot of the step
             const int nvalid = L - (t0 + i * kStep);
-            const int nv = nvalid - th * kHalf;  // valid tokens of this half
-            float t[kHalf];
-            if (!failed) {
-              const bool w = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err,
-                                       kSiteSFull, gi);
-              failed = !__all_sync(0xffffffffu, w);
-            }
-            if (!failed) {
-              tc_fence_after();
-              tmem_ld32(tS + sb * 64, t);
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_s_read(sb));
-              const bool w = mbar_wait<true>(bar_x_full(xs), (gi >> 1) & 1, abort_flag, err,
-                                             kSiteXchg, gi);
-              failed = !__all_sync(0xffffffffu, w);
-            }
-            if (!failed) {
+            bool w = mbar_wait(bar_s_full(b), (gi >> 1) & 1, abort_flag, err, kSiteSFull, gi);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc_fence_after();
+            float t[kStep];
+            tmem_ld64(tS + b * 64, t);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_s_read(b));
+            w = mbar_wait<true>(bar_x_full(b), (gi >> 1) & 1, abort_flag, err, kSiteXchg, gi);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            {
               // the score: this CTA's partial plus the peer's partial
-              const uint8_t* xin = smem + kXOff + xs * kXMsgBytes + j * 16;
+              const uint8_t* xin = smem + kXOff + b * kXMsgBytes + j * 16;
 #pragma unroll
-              for (int c = 0; c < kHalf; c += 4) {
+              for (int c = 0; c < kStep; c += 4) {
                 const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
-                t[c] += pv.x; t[c + 1] += pv.y; t[c + 2] += pv.z; t[c + 3] += pv.w;
-              }
-              __syncwarp();
-              if (lane == 0) {
-                mbar_arrive(bar_x_read(xs));
-                if (first_of_pair) mbar_arrive_expect_tx(bar_x_full(xs), kXMsgBytes);
+                fadd2_acc(t[c], t[c + 1], pv.x, pv.y);
+                fadd2_acc(t[c + 2], t[c + 3], pv.z, pv.w);
               }
             }
-            uint32_t p[kHalf / 2];
-            float alpha = 1.f;
-            bool resc = false;
-            // Fast path (whole page visible, reference set, scale >= 0): P =
-            // 2^(scale*s - m_ref) with the current reference, kept while every
-            // thread's half-row sum is at most 2^16 (which bounds every P).
-            bool fast = !failed && __all_sync(0xffffffffu, nvalid >= kStep && m_ref != -INFINITY &&
-                                                              scale_log2 >= 0.f);
-            float rs = 0.f;
-            if (fast) {
-              float rr[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) rr[u] = 0.f;
-              const float nm = -m_ref;
-#pragma unroll
-              for (int c = 0; c < kHalf; c += 8) {
-                float tv[8], pv[8];
-#pragma unroll
-                for (int u = 0; u < 8; u += 2)
-                  ffma2(tv[u], tv[u + 1], t[c + u], t[c + u + 1], scale_log2, scale_log2, nm, nm);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
-#pragma unroll
-                for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
-#pragma unroll
-                for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
-              }
-              rs = ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
-              fast = rs <= 65536.f;
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(bar_x_read(b));
+              if (first_of_pair) mbar_arrive_expect_tx(bar_x_full(b), kXMsgBytes);  // step gi + 2
             }
-            if (named_barrier_any(1, 128, failed || !fast)) {
-              // slow path (or a failure somewhere): the step from its exact
-              // row max over both token halves
-              float mx = -INFINITY;
-              if (!failed) {
+            // log2-scaled scores (tokens past the end: -inf) and their row max
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+            if (nvalid >= kStep) {
 #pragma unroll
-                for (int c = 0; c < kHalf; ++c) {
-                  t[c] = (c < nv) ? t[c] * scale_log2 : -INFINITY;
-                  mx = fmaxf(mx, t[c]);
-                }
-                pmax[((gi & 1) * 2 + th) * kOwn + j] = mx;
+              for (int c = 0; c < kStep; c += 4) {
+                ffma2(t[c], t[c + 1], t[c], t[c + 1], scale_log2, scale_log2, 0.f, 0.f);
+                ffma2(t[c + 2], t[c + 3], t[c + 2], t[c + 3], scale_log2, scale_log2, 0.f, 0.f);
+                mx0 = fmax3(mx0, t[c], t[c + 1]);
+                mx1 = fmax3(mx1, t[c + 2], t[c + 3]);
               }
-              if (named_barrier_any(1, 128, failed)) {
-                ok = false;
-                break;
-              }
-              const float mt = fmaxf(mx, pmax[((gi & 1) * 2 + (th ^ 1)) * kOwn + j]);
-              const float m_new = fmaxf(m_ref, mt);
-              resc = m_new > m_ref + kRescaleThreshold;
-              if (resc) {
-                alpha = fast_exp2(m_ref - m_new);
-                m_ref = m_new;
-                l *= alpha;
-              }
-              const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-              float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-#pragma unroll
-              for (int c = 0; c < kHalf; c += 4) {
-                const float p0 = fast_exp2(t[c] - m_use);
-                const float p1 = fast_exp2(t[c + 1] - m_use);
-                const float p2 = fast_exp2(t[c + 2] - m_use);
-                const float p3 = fast_exp2(t[c + 3] - m_use);
-                rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
-                p[c / 2] = pack_bf16x2(p0, p1);
-                p[c / 2 + 1] = pack_bf16x2(p2, p3);
-              }
-              l += (rs0 + rs1) + (rs2 + rs3);
             } else {
-              l += rs;
-            }
-            // O rows of these heads (this warp's columns): rescaled once the
-            // previous step's PV is done on this CTA
-            if (!failed && i > 0 && __any_sync(0xffffffffu, resc)) {
-              const int gp = gi - 1;
-              const bool w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
-                                             abort_flag, err, kSitePvDone, gi);
-              failed = !__all_sync(0xffffffffu, w);
-              if (!failed) {
-                tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                  float ov[32];
-                  tmem_ld32(tO + c, ov);
-                  uint32_t ou[32];
 #pragma unroll
-                  for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * alpha);
-                  tmem_st32(tO + c, ou);
-                }
-                tmem_st_wait();
+              for (int c = 0; c < kStep; ++c) {
+                t[c] = (c < nvalid) ? t[c] * scale_log2 : -INFINITY;
+                mx0 = fmaxf(mx0, t[c]);
               }
+            }
+            const float mx = fmaxf(mx0, mx1);
+            // the running max after the previous step, published by the warp
+            // of the other parity (a segment starts from -inf)
+            float m_prev = -INFINITY;
+            if (i > 0) {
+              const int gp = gi - 1;
+              w = mbar_wait(bar_m_ready(gp & 1), (gp >> 1) & 1, abort_flag, err, kSiteXchg, gi);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+              m_prev = mpub[(gp & 1) * kOwn + j];
+            }
+            // catch up with rescales made at steps of the other parity
+            if (m_prev > m_known) {
+              l *= fast_exp2(m_known - m_prev);
+              m_known = m_prev;
+            }
+            // lazy rescale: the reference moves only when the row max passes
+            // it by more than the threshold (P then stays below 2^threshold)
+            const float m_new = fmaxf(m_prev, mx);
+            const bool resc = m_new > m_prev + kRescaleThreshold;
+            const float alpha = resc ? fast_exp2(m_prev - m_new) : 1.f;  // 0 from -inf
+            if (resc) {
+              l *= alpha;
+              m_known = m_new;
+            }
+            mpub[b * kOwn + j] = m_known;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_m_ready(b));
+            const float nm = (m_known == -INFINITY) ? 0.f : -m_known;
+            uint32_t p[kStep / 2];
+            float rr[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kStep; c += 8) {
+              float tv[8], pv[8];
+#pragma unroll
+              for (int u = 0; u < 8; u += 2)
+                ffma2(tv[u], tv[u + 1], t[c + u], t[c + u + 1], 1.f, 1.f, nm, nm);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+#pragma unroll
+              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+            }
+            l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+            // O rows of these heads: rescaled once the previous step's PV is
+            // done on this CTA
+            if (i > 0 && __any_sync(0xffffffffu, resc)) {
+              const int gp = gi - 1;
+              w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
+                                  abort_flag, err, kSitePvDone, gi);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+              tc_fence_after();
+              rescale_o(alpha);
             }
             // the step's P slot is free once both CTAs' PV of step gi - 2 is done
-            if (!failed && gi >= kPSlots) {
+            if (gi >= kPSlots) {
               const int gp = gi - kPSlots;
-              const bool w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
-                                             abort_flag, err, kSiteXfree, gi);
-              failed = !__all_sync(0xffffffffu, w);
+              w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
+                                  abort_flag, err, kSiteXfree, gi);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
-            if (!failed) {
-              const int patom = (gi & 1) * kPSlotBytes + th * kPAtomBytes;
-              uint8_t* prow = smem + kPOff + patom + h * 64;
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              uint8_t* prow = smem + kPOff + b * kPSlotBytes + a * kPAtomBytes + h * 64;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) =
-                    make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
-              // the peer scales its O rows of these heads by the same factor
-              if (th == 0)
-                st_async_b32(peer_alpha + (gi & 1) * kOwn * 4, __float_as_uint(alpha),
-                             peer_xp_full0 + 8u * (gi & 1));
-              // Tokens past the end contribute exactly zero even if the cache
-              // tail holds non-finite bytes: clear those V rows of this CTA's
-              // stage before its PV reads them (p_full waits for all four
-              // softmax warps).
-              if (nvalid < kStep) {
-                uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
-                const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
-                for (int e = st; e < zrows * 4 * 8; e += 128) {
-                  const int a = e / (zrows * 8), rem = e % (zrows * 8);
-                  const int rr = nvalid + rem / 8, ch = rem % 8;
-                  *reinterpret_cast<uint4*>(vst + a * kKAtomBytes + rr * 128 + ch * 16) =
-                      make_uint4(0u, 0u, 0u, 0u);
-                }
+                    make_uint4(p[a * 16 + 4 * c], p[a * 16 + 4 * c + 1], p[a * 16 + 4 * c + 2],
+                               p[a * 16 + 4 * c + 3]);
+            }
+            // the peer scales its O rows of these heads by the same factor
+            st_async_b32(peer_alpha + b * kOwn * 4, __float_as_uint(alpha),
+                         peer_xp_full0 + 8u * b);
+            // Tokens past the end contribute exactly zero even if the cache
+            // tail holds non-finite bytes: clear those V rows of this CTA's
+            // stage before its PV reads them (p_full waits for both softmax
+            // warps of the step).
+            if (nvalid < kStep) {
+              uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
+              const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
+              for (int e = (sub & 1) * 32 + lane; e < zrows * 4 * 8; e += 64) {
+                const int a = e / (zrows * 8), rem = e % (zrows * 8);
+                const int rr2 = nvalid + rem / 8, ch = rem % 8;
+                *reinterpret_cast<uint4*>(vst + a * kKAtomBytes + rr2 * 128 + ch * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
               }
-              fence_proxy_async_smem();
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) {
-                const int off = patom + sub * 32 * 64;  // this warp's 32 rows of the atom
-                bulk_copy_to_peer(peer_p + off, sP + off, kPWarpBytes,
-                                  peer_xp_full0 + 8u * (gi & 1));
-                mbar_arrive(bar_p_full(gi & 1));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int a = 0; a < 2; ++a) {
+                const int off = b * kPSlotBytes + a * kPAtomBytes + sub * kPWarpBytes;
+                bulk_copy_to_peer(peer_p + off, sP + off, kPWarpBytes, peer_xp_full0 + 8u * b);
               }
+              mbar_arrive(bar_p_full(b));
             }
           }
-          if (ok) {
-            // the row sums over both token halves; the peer gets them for its
-            // O rows of these heads
-            lpart[th * kOwn + j] = l;
-            if (named_barrier_any(1, 128, failed)) {
+          if (!ok) break;
+          // The row sum over the segment from both parities' shares (each
+          // relative to its warp's last reference); the peer gets it for its
+          // O rows of these heads.
+          {
+            float* mine = lpart + ((seg_i & 1) * 2 + par) * kOwn * 2;
+            mine[j] = l;
+            mine[kOwn + j] = m_known;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_seg_done);
+            const bool w = mbar_wait(bar_seg_done, seg_i & 1, abort_flag, err, kSiteXchg, seg_i);
+            if (!__all_sync(0xffffffffu, w)) {
               ok = false;
-            } else {
-              const float lt = lpart[j] + lpart[kOwn + j];
-              if (th == 0)
-                st_async_b32(peer_lfin + (seg_i & 1) * kOwn * 4, __float_as_uint(lt),
-                             peer_lfin_full0 + 8u * (seg_i & 1));
-              prev_m = m_ref;
-              prev_l = lt;
+              break;
             }
+            const float* s0 = lpart + ((seg_i & 1) * 2) * kOwn * 2;
+            const float* s1 = s0 + kOwn * 2;
+            const float la = s0[j], ma = s0[kOwn + j], lb = s1[j], mb = s1[kOwn + j];
+            const float mf = fmaxf(ma, mb);
+            const float lt = (ma == -INFINITY ? 0.f : la * fast_exp2(ma - mf)) +
+                             (mb == -INFINITY ? 0.f : lb * fast_exp2(mb - mf));
+            if (par == 0)
+              st_async_b32(peer_lfin + (seg_i & 1) * kOwn * 4, __float_as_uint(lt),
+                           peer_lfin_full0 + 8u * (seg_i & 1));
+            prev_m = mf;
+            prev_l = lt;
           }
         } else {
           // ================= the peer's heads =================
-          // Iteration i sends this CTA's partial S of step i (token half th)
-          // to the peer, then takes in the peer's P rows of step i - 1: their
+          // A step of this warp's parity: send this CTA's partial S of these
+          // heads to the peer, then take in the peer's P rows of the step: their
           // rescale factors are applied to this CTA's O rows of those heads
-          // before the PV of that step may run.
-          for (int i = 0; i <= n && ok; ++i) {
-            if (i < n) {
-              const int gi = g + i;
-              const int sb = gi & (kSBufs - 1);
-              const int xs = (gi & 1) * 2 + th;
-              bool w = mbar_wait(bar_s_full(sb), (gi / kSBufs) & 1, abort_flag, err, kSiteSFull,
-                                 gi);
+          // before the PV of the step may run.
+          for (int i = (par - g) & 1; i < n; i += 2) {
+            const int gi = g + i;
+            const int b = gi & 1;
+            bool w = mbar_wait(bar_s_full(b), (gi >> 1) & 1, abort_flag, err, kSiteSFull, gi);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc_fence_after();
+            float sv[kStep];
+            tmem_ld64(tS + b * 64, sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_s_read(b));
+            // The peer sends its step gi + 1 into the slot of step gi - 1 only
+            // after its softmax has read this CTA's step gi, which is sent
+            // only after this CTA's softmax has read the peer's step gi - 1.
+            if (gi >= 1) {
+              const int gp = gi - 1;
+              w = mbar_wait(bar_x_read(gp & 1), (gp >> 1) & 1, abort_flag, err, kSiteXfree, gi);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-              tc_fence_after();
-              float sv[kHalf];
-              tmem_ld32(tS + sb * 64, sv);
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_s_read(sb));
-              // The peer sends its step gi + 1 into the slot of step gi - 1 only
-              // after its softmax has read this CTA's step gi, which is sent
-              // only after this CTA's softmax has read the peer's step gi - 1.
-              if (gi >= 1) {
-                const int gp = gi - 1;
-                w = mbar_wait(bar_x_read((gp & 1) * 2 + th), (gp >> 1) & 1, abort_flag, err,
-                              kSiteXfree, gi);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-              }
-              const uint32_t dst = peer_x + xs * kXMsgBytes;
-              const uint32_t rbar = peer_x_full0 + 8u * xs;
-#pragma unroll
-              for (int c = 0; c < kHalf; c += 4)
-                st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
-                            __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
-                            __float_as_uint(sv[c + 3]), rbar);
             }
+            const uint32_t dst = peer_x + b * kXMsgBytes;
+            const uint32_t rbar = peer_x_full0 + 8u * b;
+#pragma unroll
+            for (int c = 0; c < kStep; c += 4)
+              st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
+                          __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
+                          __float_as_uint(sv[c + 3]), rbar);
+            w = mbar_wait<true>(bar_xp_full(b), (gi >> 1) & 1, abort_flag, err, kSitePFull, gi);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            if (first_of_pair && lane == 0)
+              mbar_arrive_expect_tx(bar_xp_full(b), kXpBytes);  // for step gi + 2
             if (i > 0) {
-              const int gp = g + i - 1;
-              const int pb = gp & (kPSlots - 1);
-              bool w = mbar_wait<true>(bar_xp_full(pb), (gp >> 1) & 1, abort_flag, err,
-                                       kSitePFull, gp);
-              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-              if (first_of_pair && th == 0 && lane == 0)
-                mbar_arrive_expect_tx(bar_xp_full(pb), kXpBytes);  // for step gp + 2
-              if (i > 1) {
-                const float a = alpha_in[pb * kOwn + j];
-                if (__any_sync(0xffffffffu, a != 1.f)) {
-                  const int gq = gp - 1;
-                  w = mbar_wait<true>(bar_kv_free(gq & (kStages - 1)), (gq / kStages) & 1,
-                                      abort_flag, err, kSitePvDone, gp);
-                  if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                  tc_fence_after();
-#pragma unroll 1
-                  for (int c = 0; c < 128; c += 32) {
-                    float ov[32];
-                    tmem_ld32(tO + c, ov);
-                    uint32_t ou[32];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) ou[u] = __float_as_uint(ov[u] * a);
-                    tmem_st32(tO + c, ou);
-                  }
-                  tmem_st_wait();
-                }
+              const float a = alpha_in[b * kOwn + j];
+              if (__any_sync(0xffffffffu, a != 1.f)) {
+                const int gp = gi - 1;
+                w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
+                                    abort_flag, err, kSitePvDone, gi);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+                rescale_o(a);
               }
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_p_full(pb));
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p_full(b));
           }
         }
         if (!ok) break;
