@@ -108,9 +108,9 @@ constexpr int kMpubOff = kLfinOff + 2 * kOwn * 4;          // [step parity][64] 
 constexpr int kLpartOff = kMpubOff + 2 * kOwn * 4;         // [segment parity][step parity][l | m]
 constexpr int kBarOff = kLpartOff + 2 * 2 * kOwn * 8;
 // barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[2], x_read[2],
-// p_full[2], xp_full[2], lfin_full[2], m_ready[2], q_full, q_free, o_free,
-// seg_done, drain_s, drain_pv
-constexpr int kNumBars = 2 * kStages + 2 * kSBufs + 2 * kXSlots + 4 * kPSlots + 6;
+// p_full[2], xp_full[2], lfin_full[2], m_ready[2], kv_empty[S], q_full, q_free,
+// o_free, seg_done, drain_s, drain_pv
+constexpr int kNumBars = 3 * kStages + 2 * kSBufs + 2 * kXSlots + 4 * kPSlots + 6;
 constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -477,9 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr int kBarP = kBarX + 2 * kXSlots;
   auto bar_kv_full = [&](int s) { return bar0 + 8u * s; };
   // kv_free(s) completes when the PV of the stage's step is done on BOTH CTAs
-  // (each PV commit is multicast): it frees the stage for the producer, the P
-  // slot of the step two later, and it is how the O rescales and the
-  // epilogue learn that a PV is done.
+  // (that PV commit is multicast): it frees the P slot of the step two later.
   auto bar_kv_free = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto bar_s_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
   auto bar_s_read = [&](int b) { return bar0 + 8u * (2 * kStages + kSBufs + b); };
@@ -491,13 +489,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // m_ready(b): the softmax warps of a step of parity b have published the
   // running max after it (the next step's warps need it)
   auto bar_m_ready = [&](int b) { return bar0 + 8u * (kBarP + 3 * kPSlots + b); };
-  const uint32_t bar_q_full = bar0 + 8u * (kBarP + 4 * kPSlots);
+  // kv_empty(s): the PV of the stage's step is done on this CTA: the stage is
+  // free for the producer, and the O rescales and the epilogue learn from it
+  // that a PV is done.
+  auto bar_kv_empty = [&](int s) { return bar0 + 8u * (kBarP + 4 * kPSlots + s); };
+  const uint32_t bar_q_full = bar0 + 8u * (kBarP + 4 * kPSlots + kStages);
   const uint32_t bar_q_free = bar_q_full + 8;
   const uint32_t bar_o_free = bar_q_full + 16;
   const uint32_t bar_seg_done = bar_q_full + 24;
   const uint32_t bar_drain_s = bar_q_full + 32;
   const uint32_t bar_drain_pv = bar_q_full + 40;
-  static_assert(kBarP + 4 * kPSlots + 6 == kNumBars, "barrier count");
+  static_assert(kBarP + 4 * kPSlots + kStages + 6 == kNumBars, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -507,6 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_free(s), 2);
+      mbar_init(bar_kv_empty(s), 1);
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar_s_full(b), 1);
@@ -571,8 +574,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int t_end = min(s.p1 * kPage, L);
           for (int t = s.p0 * kPage; t < t_end; t += kStep, ++g) {
             const int slot = g % kStages, use = g / kStages;
+            // the page's table entry is read while the stage is still in use
+            int blk = block_table[(size_t)s.b * max_blocks + t / kPage];
             if (use > 0) {
-              ok = mbar_wait(bar_kv_free(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
+              ok = mbar_wait(bar_kv_empty(slot), (use - 1) & 1, abort_flag, err, kSiteKvEmpty, g);
               if (!ok) break;
             }
             if (g == skip_step) {
@@ -580,7 +585,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               issued = g + 1;
               continue;
             }
-            int blk = block_table[(size_t)s.b * max_blocks + t / kPage];
             if (blk < 0 || blk >= num_blocks) {
               record_error(err, ATTN_ERR_BAD_BLOCK_TABLE, s.b, t / kPage);
               blk = 0;  // never read outside the pool
@@ -708,6 +712,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kStep / 16; ++kk)
               mma_ss(tO, pd + (uint64_t)(((kk >> 1) * kPAtomBytes + (kk & 1) * 32) >> 4),
                      vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (i | kk) != 0);
+            tc_commit(bar_kv_empty(slot));
             tc_commit_mc(bar_kv_free(slot), 0x3);
           }
           if (!ok) break;
@@ -876,9 +881,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- the previous segment's epilogue overlaps this segment's first S
         if (prev_b >= 0) {
           ok = __all_sync(0xffffffffu,
-                          mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)),
-                                          (prev_last / kStages) & 1, abort_flag, err,
-                                          kSitePvDone, prev_seg));
+                          mbar_wait(bar_kv_empty(prev_last & (kStages - 1)),
+                                    (prev_last / kStages) & 1, abort_flag, err, kSitePvDone,
+                                    prev_seg));
           if (!ok) break;
           tc_fence_after();
           ok = epilogue();
@@ -985,8 +990,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // done on this CTA
             if (i > 0 && __any_sync(0xffffffffu, resc)) {
               const int gp = gi - 1;
-              w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
-                                  abort_flag, err, kSitePvDone, gi);
+              w = mbar_wait(bar_kv_empty(gp & (kStages - 1)), (gp / kStages) & 1,
+                            abort_flag, err, kSitePvDone, gi);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
               tc_fence_after();
               rescale_o(alpha);
@@ -1103,8 +1108,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const float a = alpha_in[b * kOwn + j];
               if (__any_sync(0xffffffffu, a != 1.f)) {
                 const int gp = gi - 1;
-                w = mbar_wait<true>(bar_kv_free(gp & (kStages - 1)), (gp / kStages) & 1,
-                                    abort_flag, err, kSitePvDone, gi);
+                w = mbar_wait(bar_kv_empty(gp & (kStages - 1)), (gp / kStages) & 1,
+                              abort_flag, err, kSitePvDone, gi);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
                 rescale_o(a);
@@ -1125,8 +1130,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     if (ok && prev_b >= 0) {
-      ok = mbar_wait<true>(bar_kv_free(prev_last & (kStages - 1)), (prev_last / kStages) & 1,
-                           abort_flag, err, kSitePvDone, prev_seg);
+      ok = mbar_wait(bar_kv_empty(prev_last & (kStages - 1)), (prev_last / kStages) & 1,
+                     abort_flag, err, kSitePvDone, prev_seg);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
