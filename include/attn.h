@@ -399,8 +399,9 @@ ATTN_API int attn_fwd_tf32x3_test_skip_load(const float* q, const float* k, cons
  * which then never receives rank 1's partial scores for the step, runs out
  * in its own bounded wait; the kernel records ATTN_ERR_DEVICE_TIMEOUT; both
  * CTAs unwind, meet at the final cluster barrier (an aborted CTA waits 50 us
- * first, so that no partial-score store is in flight towards a CTA that has
- * left) and free their tensor memory.  attn_device_status() returns the code.
+ * first, so that no partial-score store or P-row copy is in flight towards a
+ * CTA that has left) and free their tensor memory.  attn_device_status()
+ * returns the code.
  * Clusters with fewer steps finish normally.  Output contents are
  * unspecified.  Not for production use.
  */
