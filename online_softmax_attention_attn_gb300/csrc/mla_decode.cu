@@ -73,14 +73,15 @@ constexpr int kSBufs = 2;                 // TMEM S buffers (64 columns each)
 static_assert((kStages & (kStages - 1)) == 0 && (kSBufs & (kSBufs - 1)) == 0 &&
                   (kRopeSlots & (kRopeSlots - 1)) == 0,
               "ring positions are taken with masks");
-// A partial-S message: one step for the 64 heads of the receiving CTA,
-// [token quad][head][4 tokens] fp32: 16 B per head and quad, so
+// A partial-S message: one 32-token half of a step for the 64 heads of the
+// receiving CTA, [token quad][head][4 tokens] fp32: 16 B per head and quad, so
 // one warp store covers 512 contiguous bytes (contiguous remote stores move
 // about twice the bytes per clock of row-scattered ones) and each head's
 // reads are conflict-free.
 constexpr int kXQuadBytes = kOwn * 16;                 // 1 KB
-constexpr int kXMsgBytes = (kStep / 4) * kXQuadBytes;  // 16 KB
-constexpr int kXSlots = 2;                             // two steps
+constexpr int kXHalf = 32;                             // tokens per message
+constexpr int kXMsgBytes = (kXHalf / 4) * kXQuadBytes;  // 8 KB
+constexpr int kXSlots = 2 * (kStep / kXHalf);           // two steps x two halves
 // P of one step in shared memory (the A operand of the PV MMAs): two K-major
 // atoms of 32 tokens (64-byte rows, 64-byte swizzle) over the 128 head rows.
 // A warp's 32 rows of one atom are 2 KB contiguous, which is what it copies
@@ -110,7 +111,7 @@ constexpr int kBarOff = kLpartOff + 2 * 2 * kOwn * 8;
 // barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[2], x_read[2],
 // p_full[2], xp_full[2], lfin_full[2], m_ready[2], kv_empty[S], q_full, q_free,
 // o_free, seg_done, drain_s, drain_pv
-constexpr int kNumBars = 3 * kStages + 2 * kSBufs + 2 * kXSlots + 4 * kPSlots + 6;
+constexpr int kNumBars = 3 * kStages + 3 * kSBufs + kXSlots + 4 * kPSlots + 6;
 constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -474,7 +475,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t sP = base + kPOff;
   const uint32_t bar0 = base + kBarOff;
   constexpr int kBarX = 2 * kStages + 2 * kSBufs;
-  constexpr int kBarP = kBarX + 2 * kXSlots;
+  constexpr int kBarP = kBarX + kXSlots + kSBufs;
   auto bar_kv_full = [&](int s) { return bar0 + 8u * s; };
   // kv_free(s) completes when the PV of the stage's step is done on BOTH CTAs
   // (that PV commit is multicast): it frees the P slot of the step two later.
@@ -515,10 +516,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_s_full(b), 1);
       mbar_init(bar_s_read(b), 4);  // the four compute warps of the step's parity
     }
-    for (int x = 0; x < kXSlots; ++x) {
-      mbar_init(bar_x_full(x), 1);
-      mbar_init(bar_x_read(x), 2);  // the two softmax warps of the step's parity
-    }
+    for (int x = 0; x < kXSlots; ++x) mbar_init(bar_x_full(x), 1);
+    for (int b = 0; b < kSBufs; ++b) mbar_init(bar_x_read(b), 2);  // the step's softmax warps
     for (int b = 0; b < kPSlots; ++b) {
       mbar_init(bar_p_full(b), 4);
       mbar_init(bar_xp_full(b), 1);
@@ -906,38 +905,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_s_read(b));
-            w = mbar_wait<true>(bar_x_full(b), (gi >> 1) & 1, abort_flag, err, kSiteXchg, gi);
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            {
-              // the score: this CTA's partial plus the peer's partial
-              const uint8_t* xin = smem + kXOff + b * kXMsgBytes + j * 16;
+            // The score is this CTA's partial plus the peer's.  The peer's
+            // arrives in two 32-token halves: the first is summed, scaled
+            // (log2 units; tokens past the end -inf) and maxed while the
+            // second is still on its way.
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+            bool xok = true;
 #pragma unroll
-              for (int c = 0; c < kStep; c += 4) {
-                const float4 pv = *reinterpret_cast<const float4*>(xin + (c / 4) * kXQuadBytes);
+            for (int hx = 0; hx < 2; ++hx) {
+              const int xs = b * 2 + hx;
+              xok = __all_sync(0xffffffffu, mbar_wait<true>(bar_x_full(xs), (gi >> 1) & 1,
+                                                              abort_flag, err, kSiteXchg, gi));
+              if (!xok) break;
+              const uint8_t* xin = smem + kXOff + xs * kXMsgBytes + j * 16;
+#pragma unroll
+              for (int c = hx * kXHalf; c < (hx + 1) * kXHalf; c += 4) {
+                const float4 pv =
+                    *reinterpret_cast<const float4*>(xin + ((c - hx * kXHalf) / 4) * kXQuadBytes);
                 fadd2_acc(t[c], t[c + 1], pv.x, pv.y);
                 fadd2_acc(t[c + 2], t[c + 3], pv.z, pv.w);
               }
+              if (nvalid >= kStep) {
+#pragma unroll
+                for (int c = hx * kXHalf; c < (hx + 1) * kXHalf; c += 4) {
+                  ffma2(t[c], t[c + 1], t[c], t[c + 1], scale_log2, scale_log2, 0.f, 0.f);
+                  ffma2(t[c + 2], t[c + 3], t[c + 2], t[c + 3], scale_log2, scale_log2, 0.f, 0.f);
+                  mx0 = fmax3(mx0, t[c], t[c + 1]);
+                  mx1 = fmax3(mx1, t[c + 2], t[c + 3]);
+                }
+              } else {
+#pragma unroll
+                for (int c = hx * kXHalf; c < (hx + 1) * kXHalf; ++c) {
+                  t[c] = (c < nvalid) ? t[c] * scale_log2 : -INFINITY;
+                  mx0 = fmaxf(mx0, t[c]);
+                }
+              }
+            }
+            if (!xok) {
+              ok = false;
+              break;
             }
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(bar_x_read(b));
-              if (first_of_pair) mbar_arrive_expect_tx(bar_x_full(b), kXMsgBytes);  // step gi + 2
-            }
-            // log2-scaled scores (tokens past the end: -inf) and their row max
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-            if (nvalid >= kStep) {
-#pragma unroll
-              for (int c = 0; c < kStep; c += 4) {
-                ffma2(t[c], t[c + 1], t[c], t[c + 1], scale_log2, scale_log2, 0.f, 0.f);
-                ffma2(t[c + 2], t[c + 3], t[c + 2], t[c + 3], scale_log2, scale_log2, 0.f, 0.f);
-                mx0 = fmax3(mx0, t[c], t[c + 1]);
-                mx1 = fmax3(mx1, t[c + 2], t[c + 3]);
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < kStep; ++c) {
-                t[c] = (c < nvalid) ? t[c] * scale_log2 : -INFINITY;
-                mx0 = fmaxf(mx0, t[c]);
+              if (first_of_pair) {  // both halves, for step gi + 2
+                mbar_arrive_expect_tx(bar_x_full(b * 2), kXMsgBytes);
+                mbar_arrive_expect_tx(bar_x_full(b * 2 + 1), kXMsgBytes);
               }
             }
             const float mx = fmaxf(mx0, mx1);
@@ -968,24 +981,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_m_ready(b));
             const float nm = (m_known == -INFINITY) ? 0.f : -m_known;
-            uint32_t p[kStep / 2];
-            float rr[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kStep; c += 8) {
-              float tv[8], pv[8];
-#pragma unroll
-              for (int u = 0; u < 8; u += 2)
-                ffma2(tv[u], tv[u + 1], t[c + u], t[c + u + 1], 1.f, 1.f, nm, nm);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
-#pragma unroll
-              for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
-            }
-            l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
             // O rows of these heads: rescaled once the previous step's PV is
             // done on this CTA
             if (i > 0 && __any_sync(0xffffffffu, resc)) {
@@ -1003,43 +998,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                   abort_flag, err, kSiteXfree, gi);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
+            // the peer scales its O rows of these heads by the same factor
+            st_async_b32(peer_alpha + b * kOwn * 4, __float_as_uint(alpha),
+                         peer_xp_full0 + 8u * b);
+            // P one 32-token atom at a time; each atom's rows of these heads go
+            // to the peer as soon as they are written
+            float rr[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rr[u] = 0.f;
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
+              uint32_t p[16];
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                float tv[8], pv[8];
+#pragma unroll
+                for (int u = 0; u < 8; u += 2)
+                  ffma2(tv[u], tv[u + 1], t[a * 32 + c + u], t[a * 32 + c + u + 1], 1.f, 1.f, nm,
+                        nm);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pv[u] = fast_exp2(tv[u]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) fadd2_acc(rr[u], rr[u + 1], pv[u], pv[u + 1]);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) p[(c + u) / 2] = pack_bf16x2(pv[u], pv[u + 1]);
+              }
               uint8_t* prow = smem + kPOff + b * kPSlotBytes + a * kPAtomBytes + h * 64;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) =
-                    make_uint4(p[a * 16 + 4 * c], p[a * 16 + 4 * c + 1], p[a * 16 + 4 * c + 2],
-                               p[a * 16 + 4 * c + 3]);
-            }
-            // the peer scales its O rows of these heads by the same factor
-            st_async_b32(peer_alpha + b * kOwn * 4, __float_as_uint(alpha),
-                         peer_xp_full0 + 8u * b);
-            // Tokens past the end contribute exactly zero even if the cache
-            // tail holds non-finite bytes: clear those V rows of this CTA's
-            // stage before its PV reads them (p_full waits for both softmax
-            // warps of the step).
-            if (nvalid < kStep) {
-              uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
-              const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
-              for (int e = (sub & 1) * 32 + lane; e < zrows * 4 * 8; e += 64) {
-                const int a = e / (zrows * 8), rem = e % (zrows * 8);
-                const int rr2 = nvalid + rem / 8, ch = rem % 8;
-                *reinterpret_cast<uint4*>(vst + a * kKAtomBytes + rr2 * 128 + ch * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                    make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+              // Tokens past the end contribute exactly zero even if the cache
+              // tail holds non-finite bytes: clear those V rows of this CTA's
+              // stage before its PV reads them (p_full waits for both softmax
+              // warps of the step).
+              if (a == 1 && nvalid < kStep) {
+                uint8_t* vst = smem + kStageOff + (gi % kStages) * kStageBytes;
+                const int zrows = kStep - nvalid;  // rows [nvalid, 64) of atoms 0..3
+                for (int e = (sub & 1) * 32 + lane; e < zrows * 4 * 8; e += 64) {
+                  const int za = e / (zrows * 8), rem = e % (zrows * 8);
+                  const int rr2 = nvalid + rem / 8, ch = rem % 8;
+                  *reinterpret_cast<uint4*>(vst + za * kKAtomBytes + rr2 * 128 + ch * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+                }
               }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-              for (int a = 0; a < 2; ++a) {
+              fence_proxy_async_smem();
+              if (a == 1) tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
                 const int off = b * kPSlotBytes + a * kPAtomBytes + sub * kPWarpBytes;
                 bulk_copy_to_peer(peer_p + off, sP + off, kPWarpBytes, peer_xp_full0 + 8u * b);
+                if (a == 1) mbar_arrive(bar_p_full(b));
               }
-              mbar_arrive(bar_p_full(b));
             }
+            l += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
           }
           if (!ok) break;
           // The row sum over the segment from both parities' shares (each
@@ -1093,13 +1105,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               w = mbar_wait(bar_x_read(gp & 1), (gp >> 1) & 1, abort_flag, err, kSiteXfree, gi);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
-            const uint32_t dst = peer_x + b * kXMsgBytes;
-            const uint32_t rbar = peer_x_full0 + 8u * b;
 #pragma unroll
-            for (int c = 0; c < kStep; c += 4)
-              st_async_v4(dst + (c / 4) * kXQuadBytes, __float_as_uint(sv[c]),
-                          __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
-                          __float_as_uint(sv[c + 3]), rbar);
+            for (int hx = 0; hx < 2; ++hx) {
+              const uint32_t dst = peer_x + (b * 2 + hx) * kXMsgBytes;
+              const uint32_t rbar = peer_x_full0 + 8u * (b * 2 + hx);
+#pragma unroll
+              for (int c = hx * kXHalf; c < (hx + 1) * kXHalf; c += 4)
+                st_async_v4(dst + ((c - hx * kXHalf) / 4) * kXQuadBytes, __float_as_uint(sv[c]),
+                            __float_as_uint(sv[c + 1]), __float_as_uint(sv[c + 2]),
+                            __float_as_uint(sv[c + 3]), rbar);
+            }
             w = mbar_wait<true>(bar_xp_full(b), (gi >> 1) & 1, abort_flag, err, kSitePFull, gi);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             if (first_of_pair && lane == 0)
