@@ -16,22 +16,28 @@
 //   * O = 128 heads x 512 fp32 would fill all of one SM's TMEM, so a CLUSTER
 //     OF TWO CTAs shares each work item by columns: rank 0 owns latent
 //     columns [0,256) and RoPE columns [512,544), rank 1 owns [256,512) and
-//     [544,576) (18 S MMAs each per step).  Each
-//     CTA TMA-loads only its own columns of every cached row (HBM is read
-//     once) and computes a partial S over them with its share of q held in
-//     TMEM.  Four exchange warps push each partial S tile into the peer's
-//     shared memory with st.async (arrival counted in bytes on the peer's
-//     mbarrier, so no thread issues a cluster-scope fence); the four softmax
-//     warps add the two partials in the same order on both CTAs and run the
-//     identical softmax; each CTA accumulates its 256 columns of O = P V in
-//     TMEM (V is the same shared-memory bytes as K).
+//     [544,576) (18 S MMAs each per step).  Each CTA TMA-loads only its own
+//     columns of every cached row (HBM is read once) and computes a partial S
+//     over them for all 128 heads with its share of q held in TMEM.
+//   * The softmax of each head runs on one CTA only: rank r owns heads
+//     64 r .. 64 r + 63.  A CTA pushes its partial S of the peer's heads into
+//     the peer's shared memory with st.async (two 32-token messages per step,
+//     arrival counted in bytes on the peer's mbarrier), adds the peer's
+//     partial of its own heads to its own, runs their online softmax, writes
+//     their bf16 P rows into a shared-memory P tile and bulk-copies those rows
+//     into the peer's tile, with each head's rescale factor.  Both CTAs then
+//     accumulate their 256 columns of O = P V in TMEM with P from shared
+//     memory (V is the same shared-memory bytes as K), after applying the
+//     peer's factors to their O rows of the peer's heads.
 //   * Each 64-token page is one step (S MMAs with N=64) through a 4-stage TMA
 //     ring of the CTA's c_kv atoms and its 32 RoPE columns; the block table is
-//     read on the device and bounds-checked.  Two S
-//     buffers in TMEM let the tensor core compute step g+1 while the softmax
-//     of step g runs; the partial S travels in two 32-token halves.  Warps:
-//     0-3 softmax + epilogue, 4 TMA producer, 5 MMA issuer, 6-9 partial-S
-//     exchange.
+//     read on the device and bounds-checked.  Two S buffers in TMEM; since P
+//     lives in shared memory, an S buffer is free as soon as it has been
+//     read, and S and PV are issued by two threads.  Warps 0-7: softmax of the
+//     own heads or service of the peer's heads, by TMEM lane quarter, the two
+//     step parities in ping-pong; 8 TMA producer; 9 S-MMA issuer; 10 PV-MMA
+//     issuer.  Each PV commit is multicast to both CTAs: a P slot is reused
+//     once both CTAs' PVs of the step are done.
 //   * Work is a list of page ranges ("chunks") of the flat page order, one
 //     chunk per cluster at a time (persistent).  The device planner either
 //     gives each sequence its own chunk (no partials) or cuts the flat order
