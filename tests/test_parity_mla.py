@@ -165,6 +165,26 @@ def test_scores_jump_on_a_later_page():
     _check(q, kv, table, sl, o, lse)
 
 
+def test_heads_of_each_cta_jump_at_different_steps():
+    """The two CTAs of a decode cluster run the softmax of heads 0-63 and
+    64-127.  Heads 0-63 get a large score jump on page 5 (an odd step), heads
+    64-127 on page 8 and again on page 9 (even, then odd): each CTA moves its
+    references at its own steps, on both step parities, and the peer must
+    apply those factors to its O columns of the same heads."""
+    q, kv, table, sl = mla_inputs(3, 128, [1000, 640, 1500], seed=37)
+    q = q.float()
+    kv = kv.float()
+    q[:, :64, 0:64] += 2.0      # heads 0-63 see columns 0-63 ...
+    q[:, 64:, 64:128] += 2.0    # ... heads 64-127 columns 64-127
+    for b in range(3):
+        kv[int(table[b, 5]), :, 0:64] += 2.0     # ~27 log2 units up for heads 0-63
+        kv[int(table[b, 8]), :, 64:128] += 1.5   # ~20 up for heads 64-127 ...
+        kv[int(table[b, 9]), :, 64:128] += 3.0   # ... and ~20 more on the next page
+    q, kv = q.to(torch.bfloat16), kv.to(torch.bfloat16)
+    o, lse = _gpu(q, kv, table, sl)
+    _check(q, kv, table, sl, o, lse)
+
+
 def _all_rows(cfg):
     q, kv, table, sl = mla_config_inputs(cfg)
     o, lse = _gpu(q, kv, table, sl)
