@@ -18,10 +18,10 @@
 //               as the previous item's last S MMA of that tile is done, then
 //               K_j and V_j together into a ring of stages (128-byte
 //               swizzle), one full and one empty mbarrier per stage.  The next
-//               item is claimed from the launch's ticket counter only after
-//               this item's last K/V load is issued, so items go to the CTAs
-//               that free up first; its number reaches the other warps
-//               through a 4-slot ring in shared memory.
+//               item is claimed from the launch's ticket counter a few blocks
+//               before this one ends, so items go to the CTAs that free up
+//               first; its number reaches the other warps through a 4-slot
+//               ring in shared memory.
 //   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
 //               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
 //               O_t += P_t V_j with P read straight from TMEM as the A operand,
@@ -219,23 +219,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar_item_full(slot));
         if (item >= total_items) break;
         const Item it = decode_item<kCausal>(item, BH, N);
-        // Q_t of this item once the previous item's last S of that tile is done
-#pragma unroll
-        for (int t = 0; t < kTilesPerCta; ++t) {
-          if (it.T[t] == 0) continue;
-          if (qn[t] > 0) {
-            ok = mbar_wait(bar_q_free(t), (qn[t] - 1) & 1, abort_flag, err, kSiteQFull, k);
-            if (!ok) break;
-          }
+        // Q_t of this item once the previous item's last S of that tile is
+        // done.  Q_0 goes first, then K/V block 0, then Q_1: tile 1 runs one
+        // block longer than tile 0 at the end of a causal item, and block 0
+        // need not wait for that.
+        auto load_q = [&](int t) -> bool {
+          if (it.T[t] == 0) return true;
+          if (qn[t] > 0 &&
+              !mbar_wait(bar_q_free(t), (qn[t] - 1) & 1, abort_flag, err, kSiteQFull, k))
+            return false;
           mbar_arrive_expect_tx(bar_q_full(t), C::kTileBytes);
           for (int a = 0; a < C::kAtoms; ++a)
             tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full(t), a * 64,
                         (2 * it.pr + t) * kBM, it.bh);
           ++qn[t];
-        }
+          return true;
+        };
+        ok = load_q(0);
         if (!ok) break;
         const int Tmax = max(it.T[0], it.T[1]);
+        // The next item is claimed two blocks before this item's last K/V
+        // load (about four blocks before the item ends), so that the
+        // claim's round trip to the counter is hidden behind those loads;
+        // items still go to the CTAs that free up first.
+        const int j_claim = max(0, Tmax - 2);
+        int next = total_items;
         for (int j = 0; j < Tmax; ++j, ++kv) {
+          if (j == j_claim) next = (int)gridDim.x + atomicAdd(ticket, 1);
           const int s = kv % C::kStages;
           const int use = kv / C::kStages;
           if (use > 0) {
@@ -244,23 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j == skip_block) {
             skipped |= 1u << (kv & 31);
-            continue;
+          } else {
+            skipped &= ~(1u << (kv & 31));
+            // K_j and V_j land on one barrier
+            const uint32_t dst = sRing + s * C::kStageBytes;
+            mbar_arrive_expect_tx(bar_kv_full(s), C::kStageBytes);
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_load_3d_hint(dst + a * kAtomBytes, &tmK, bar_kv_full(s), a * 64, j * kBN,
+                               it.bh, pol_kv);
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(s), a * 64,
+                               j * kBN, it.bh, pol_kv);
           }
-          skipped &= ~(1u << (kv & 31));
-          // K_j and V_j land on one barrier
-          const uint32_t dst = sRing + s * C::kStageBytes;
-          mbar_arrive_expect_tx(bar_kv_full(s), C::kStageBytes);
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d_hint(dst + a * kAtomBytes, &tmK, bar_kv_full(s), a * 64, j * kBN, it.bh,
-                             pol_kv);
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(s), a * 64,
-                             j * kBN, it.bh, pol_kv);
+          if (j == 0) {
+            ok = load_q(1);
+            if (!ok) break;
+          }
         }
-        // The next item is claimed only now, two blocks before this one ends,
-        // so items go to the CTAs that free up first (as a launch of one CTA
-        // per item would place them).
-        if (ok) item = (int)gridDim.x + atomicAdd(ticket, 1);
+        item = next;
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA unwinds.
