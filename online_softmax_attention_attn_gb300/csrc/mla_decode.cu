@@ -103,7 +103,7 @@ constexpr uint32_t kLfinBytes = kOwn * 4;
 constexpr float kRescaleThreshold = 8.0f;
 
 constexpr int kQropeOff = 0;             // q's RoPE half (A of 2 S MMAs)
-constexpr int kRopeOff = kQropeOff + kQropeBytes;  // k_rope ring
+constexpr int kRopeOff = kQropeOff + kQropeBytes;  // the stages' k_rope slots
 constexpr int kStageOff = kRopeOff + kRopeSlots * kKropeBytes;
 static_assert(kStageOff % 1024 == 0, "swizzled stages start on 1024-byte boundaries");
 constexpr int kXOff = kStageOff + kStages * kStageBytes;
@@ -114,7 +114,7 @@ constexpr int kLfinOff = kAlphaOff + kPSlots * kOwn * 4;   // [segment parity][6
 constexpr int kMpubOff = kLfinOff + 2 * kOwn * 4;          // [step parity][64] running maxima
 constexpr int kLpartOff = kMpubOff + 2 * kOwn * 4;         // [segment parity][step parity][l | m]
 constexpr int kBarOff = kLpartOff + 2 * 2 * kOwn * 8;
-// barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[2], x_read[2],
+// barriers: kv_full[S], kv_free[S], s_full[2], s_read[2], x_full[4], x_read[2],
 // p_full[2], xp_full[2], lfin_full[2], m_ready[2], kv_empty[S], q_full, q_free,
 // o_free, seg_done, drain_s, drain_pv
 constexpr int kNumBars = 3 * kStages + 3 * kSBufs + kXSlots + 4 * kPSlots + 6;
