@@ -654,6 +654,8 @@ CONFIG_LEGS = [
     ("decode_b16", 1 << 30), ("decode_b128", 4096), ("decode_b256", 4096),
 ]
 SUSTAINED_S = 2.0
+TABLE_WARMUP = 10   # per-workload table: warm-up calls, then the median of
+TABLE_REPS = 50     # at least this many L2-flushed calls
 
 
 def time_calls(leg, reps, flush, stream):
@@ -803,6 +805,18 @@ def main():
         if pkg.attn_device_status(raise_on_error=False) != 0:
             raise SystemExit(f"device error in the sustained runs: {pkg.attn_last_error()}")
 
+    # ---- the per-workload table wants the median of at least TABLE_REPS calls
+    # after TABLE_WARMUP; the step's legs get extra reps when K is smaller
+    table_times = {}
+    if args.workload == "step" and not args.no_configs:
+        for lg in legs:
+            tt = times[id(lg)]
+            if len(tt) < TABLE_REPS:
+                tt = time_calls(lg, TABLE_REPS, flush, stream)
+            table_times[id(lg)] = tt
+        if pkg.attn_device_status(raise_on_error=False) != 0:
+            raise SystemExit(f"device error in the table reps: {pkg.attn_last_error()}")
+
     # ---- end to end through the public API with pinned host buffers: each leg in
     # its own loop (inputs copied in, the call, outputs read back, a sync)
     e2e_steps = max(3, min(args.steps, 20))
@@ -831,7 +845,7 @@ def main():
         for lg in legs:
             checks[id(lg)] = lg.oracle_check(threads, 1 << 30)
 
-    # ---- every other workload of the target list: median of K calls, the
+    # ---- every other workload of the target list: median of max(K, TABLE_REPS) calls, the
     # roofline fractions, and the output against the oracle
     configs = {}
     if args.workload == "step" and not args.no_configs:
@@ -847,10 +861,10 @@ def main():
             if not _leg_works(lg, pkg):
                 configs[name] = {"unavailable": pkg.attn_last_error()}
                 continue
-            for _ in range(3):
+            for _ in range(max(args.warmup, TABLE_WARMUP)):
                 flush.zero_()
                 lg.run()
-            tt = time_calls(lg, max(args.steps, 20), flush, stream)
+            tt = time_calls(lg, max(args.steps, TABLE_REPS), flush, stream)
             if pkg.attn_device_status(raise_on_error=False) != 0:
                 raise SystemExit(f"device error in {name}: {pkg.attn_last_error()}")
             chk = None if args.no_cpu_baseline else lg.oracle_check(threads, max_rows)
@@ -939,14 +953,15 @@ def main():
     line["gpu_launches"] = args.steps * sum(_launches(lg, pkg) for lg in legs)
     line["clocks"] = clocks
 
-    # per-workload table: the step's own legs from the timed steps, the rest
-    # measured above
+    # per-workload table: the step's own legs from the timed steps (or their
+    # extra reps), the rest measured above
     if configs or (args.workload == "step" and not args.no_configs):
         table = {}
         for name, max_rows in CONFIG_LEGS:
             if name in names:
                 lg = legs[names.index(name)]
-                table[name] = config_entry(lg, times[id(lg)], peaks, props, smax_mhz,
+                table[name] = config_entry(lg, table_times.get(id(lg), times[id(lg)]),
+                                           peaks, props, smax_mhz,
                                            checks.get(id(lg)))
             elif name in configs:
                 c = configs[name]
