@@ -12,10 +12,14 @@
 // What differs from the blog's kernel: instead of one thread per query row
 // (latency bound, section 4.2), 256 threads form a 16 x 16 grid and each
 // thread owns an 8-row x 4-key tile of S and an 8-row x 4-column tile of O,
-// so every shared-memory load feeds 8-32 FFMAs.  Rows are interleaved
+// so every shared-memory load feeds 8-32 FMAs.  Rows are interleaved
 // (r = ty + 16 i) and keys too (c = tx + 16 j), which makes the padded
-// 68-float rows bank-conflict free for 128-bit loads.  Softmax runs in base 2
-// with log2(e) folded into the Q pre-scale.
+// 68-float rows bank-conflict free for 128-bit loads.  Both products use the
+// packed two-lane FMA (fma.rn.f32x2), half the instructions of scalar FFMAs:
+// S over pairs of d (even and odd partial sums per element, added at the
+// end), PV over pairs of output columns with P kept in shared memory as
+// (p, p) pairs.  Softmax runs in base 2 with log2(e) folded into the Q
+// pre-scale.
 #include <math.h>
 
 #include "common.cuh"
@@ -28,7 +32,7 @@ constexpr int kBc = 64;
 constexpr int kThreads = 256;
 constexpr int kQPad = kD + 4;  // 68 floats: 16-byte aligned rows, shifted banks
 constexpr int kKPad = kD + 4;
-constexpr int kPPad = kBc + 4;
+constexpr int kPPad = 2 * kBc + 8;  // P stored as (p, p) pairs: 136 floats a row
 constexpr int kSmemFloats = kBr * kQPad + 2 * kBc * kKPad + 2 * kBc * kD + kBr * kPPad;
 constexpr int kSmemBytes = kSmemFloats * 4;
 
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
   float* Ks = Qs + kBr * kQPad;           // [2][Bc][68]
   float* Vs = Ks + 2 * kBc * kKPad;       // [2][Bc][64]
-  float* Ps = Vs + 2 * kBc * kD;          // [Br][68]
+  float* Ps = Vs + 2 * kBc * kD;          // [Br][136]: each P twice, (p, p)
 
   const int n_qt = (N + kBr - 1) / kBr;
   // Heaviest causal Q blocks first across all heads (longest-first order).
@@ -127,12 +131,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_commit();
     }
 
-    // ---- S = Q K^T for this thread's 8 x 4 tile (log2 units)
-    float s[8][4];
+    // ---- S = Q K^T for this thread's 8 x 4 tile (log2 units).  Packed
+    // two-lane FMAs over pairs of d: each (row, key) keeps an even-d and an
+    // odd-d partial sum, added once at the end.
+    float se[8][4], so[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) s[i][jj] = 0.f;
+      for (int jj = 0; jj < 4; ++jj) se[i][jj] = so[i][jj] = 0.f;
     const float* Kb = Ks + buf * kBc * kKPad;
 #pragma unroll 4
     for (int d4 = 0; d4 < kD / 4; ++d4) {
@@ -147,12 +153,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          s[i][jj] = fmaf(qv[i].x, kv4[jj].x, s[i][jj]);
-          s[i][jj] = fmaf(qv[i].y, kv4[jj].y, s[i][jj]);
-          s[i][jj] = fmaf(qv[i].z, kv4[jj].z, s[i][jj]);
-          s[i][jj] = fmaf(qv[i].w, kv4[jj].w, s[i][jj]);
+          gb300::ffma2(se[i][jj], so[i][jj], qv[i].x, qv[i].y, kv4[jj].x, kv4[jj].y, se[i][jj],
+                       so[i][jj]);
+          gb300::ffma2(se[i][jj], so[i][jj], qv[i].z, qv[i].w, kv4[jj].z, kv4[jj].w, se[i][jj],
+                       so[i][jj]);
         }
     }
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) s[i][jj] = se[i][jj] + so[i][jj];
 
     // ---- mask: keys past N; causal diagonal block: key > row
     const bool tail = kv0 + kBc > N;
@@ -191,39 +202,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int d = 0; d < 4; ++d) acc[i][d] *= alpha;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) Ps[(ty + 16 * i) * kPPad + tx + 16 * jj] = s[i][jj];
+      for (int jj = 0; jj < 4; ++jj)
+        *reinterpret_cast<float2*>(Ps + (ty + 16 * i) * kPPad + 2 * (tx + 16 * jj)) =
+            make_float2(s[i][jj], s[i][jj]);
     }
     __syncthreads();  // P visible
 
-    // ---- O += P V for this thread's 8 x 4 tile
+    // ---- O += P V for this thread's 8 x 4 tile: packed two-lane FMAs over
+    // pairs of output columns, P read as (p, p) pairs
     const float* Vb = Vs + buf * kBc * kD;
 #pragma unroll 2
     for (int c4 = 0; c4 < kBc / 4; ++c4) {
-      float4 pv[8], vv[4];
+      float4 pa[8], pb[8], vv[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        pv[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * kPPad + c4 * 4);
+      for (int i = 0; i < 8; ++i) {
+        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * kPPad + c4 * 8);
+        pb[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * kPPad + c4 * 8 + 4);
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         vv[kk] = *reinterpret_cast<const float4*>(Vb + (c4 * 4 + kk) * kD + tx * 4);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        acc[i][0] = fmaf(pv[i].x, vv[0].x, acc[i][0]);
-        acc[i][1] = fmaf(pv[i].x, vv[0].y, acc[i][1]);
-        acc[i][2] = fmaf(pv[i].x, vv[0].z, acc[i][2]);
-        acc[i][3] = fmaf(pv[i].x, vv[0].w, acc[i][3]);
-        acc[i][0] = fmaf(pv[i].y, vv[1].x, acc[i][0]);
-        acc[i][1] = fmaf(pv[i].y, vv[1].y, acc[i][1]);
-        acc[i][2] = fmaf(pv[i].y, vv[1].z, acc[i][2]);
-        acc[i][3] = fmaf(pv[i].y, vv[1].w, acc[i][3]);
-        acc[i][0] = fmaf(pv[i].z, vv[2].x, acc[i][0]);
-        acc[i][1] = fmaf(pv[i].z, vv[2].y, acc[i][1]);
-        acc[i][2] = fmaf(pv[i].z, vv[2].z, acc[i][2]);
-        acc[i][3] = fmaf(pv[i].z, vv[2].w, acc[i][3]);
-        acc[i][0] = fmaf(pv[i].w, vv[3].x, acc[i][0]);
-        acc[i][1] = fmaf(pv[i].w, vv[3].y, acc[i][1]);
-        acc[i][2] = fmaf(pv[i].w, vv[3].z, acc[i][2]);
-        acc[i][3] = fmaf(pv[i].w, vv[3].w, acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].x, pa[i].y, vv[0].x, vv[0].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].x, pa[i].y, vv[0].z, vv[0].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].z, pa[i].w, vv[1].x, vv[1].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].z, pa[i].w, vv[1].z, vv[1].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pb[i].x, pb[i].y, vv[2].x, vv[2].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pb[i].x, pb[i].y, vv[2].z, vv[2].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pb[i].z, pb[i].w, vv[3].x, vv[3].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pb[i].z, pb[i].w, vv[3].z, vv[3].w, acc[i][2], acc[i][3]);
       }
     }
   }
