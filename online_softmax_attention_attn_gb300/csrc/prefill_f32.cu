@@ -6,7 +6,7 @@
 // on chip (section 1.2), O is rescaled with exp(m_old - m_new) and divided by
 // l once at the end (section 1.3), KV blocks above the diagonal are never
 // visited and only blocks crossing it are masked element by element
-// (sections 1.4 and 3.4), K/V blocks are double buffered with cp.async and
+// (sections 1.4 and 3.4), K/V blocks are prefetched with cp.async and
 // zero-filled past N while those keys get -inf (section 3.2).
 //
 // What differs from the blog's kernel: instead of one thread per query row
@@ -19,7 +19,12 @@
 // S over pairs of d (even and odd partial sums per element, added at the
 // end), PV over pairs of output columns with P kept in shared memory as
 // (p, p) pairs.  Softmax runs in base 2 with log2(e) folded into the Q
-// pre-scale.
+// pre-scale.  The CTA's two halves (warps 0-3 and 4-7, 64 interleaved rows
+// each) synchronise only among themselves and run the KV loop half a block
+// apart, so that one half's softmax overlaps the other half's FMA loops: K/V
+// blocks sit in a ring of three buffers whose loads report on a full mbarrier
+// (cp.async.mbarrier.arrive) and whose reuse waits on an empty one.  Every
+// wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
 #include <math.h>
 
 #include "common.cuh"
@@ -30,11 +35,15 @@ constexpr int kD = 64;
 constexpr int kBr = 128;
 constexpr int kBc = 64;
 constexpr int kThreads = 256;
+constexpr int kTy = 16;                 // row groups (rows interleaved by kTy)
+constexpr int kRows = kBr / kTy;        // query rows per thread
+constexpr int kKvBufs = 3;              // K/V blocks in shared memory
 constexpr int kQPad = kD + 4;  // 68 floats: 16-byte aligned rows, shifted banks
 constexpr int kKPad = kD + 4;
 constexpr int kPPad = 2 * kBc + 8;  // P stored as (p, p) pairs: 136 floats a row
-constexpr int kSmemFloats = kBr * kQPad + 2 * kBc * kKPad + 2 * kBc * kD + kBr * kPPad;
-constexpr int kSmemBytes = kSmemFloats * 4;
+constexpr int kSmemFloats =
+    kBr * kQPad + kKvBufs * kBc * kKPad + kKvBufs * kBc * kD + kBr * kPPad;
+constexpr int kSmemBytes = kSmemFloats * 4 + (2 * kKvBufs + 1) * 8 + 16;  // + barriers, flag
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -46,6 +55,11 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Copy one K and one V block [kv0, kv0 + Bc) of head bh into buffer `buf`.
@@ -73,12 +87,18 @@ template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                        const float* __restrict__ v, float* __restrict__ o,
-                       float* __restrict__ lse, int BH, int N, float qscale) {
+                       float* __restrict__ lse, int BH, int N, float qscale, int* err) {
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
-  float* Ks = Qs + kBr * kQPad;           // [2][Bc][68]
-  float* Vs = Ks + 2 * kBc * kKPad;       // [2][Bc][64]
-  float* Ps = Vs + 2 * kBc * kD;          // [Br][136]: each P twice, (p, p)
+  float* Ks = Qs + kBr * kQPad;           // [3][Bc][68]
+  float* Vs = Ks + kKvBufs * kBc * kKPad; // [3][Bc][64]
+  float* Ps = Vs + kKvBufs * kBc * kD;    // [Br][136]: each P twice, (p, p)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ps + kBr * kPPad);  // full[3], empty[3], go
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kKvBufs + 1);
+  const uint32_t bar0 = gb300::smem_u32(bars);
+  auto bar_full = [&](int b) { return bar0 + 8u * b; };
+  auto bar_empty = [&](int b) { return bar0 + 8u * (kKvBufs + b); };
+  const uint32_t bar_go = bar0 + 8u * (2 * kKvBufs);
 
   const int n_qt = (N + kBr - 1) / kBr;
   // Heaviest causal Q blocks first across all heads (longest-first order).
@@ -89,6 +109,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
+  // The two halves of the CTA (warps 0-3: ty 0-7, warps 4-7: ty 8-15) own
+  // disjoint rows and run the block loop half a block apart, so that one
+  // half's softmax overlaps the other's FMA loops.
+  const int half = ty >> 3;
+
+  if (tid == 0) {
+    for (int b = 0; b < kKvBufs; ++b) {
+      gb300::mbar_init(bar_full(b), kThreads);   // every thread's copies of the block
+      gb300::mbar_init(bar_empty(b), kThreads);  // every thread done reading it
+    }
+    gb300::mbar_init(bar_go, kThreads / 2);      // half 0 has finished its first softmax
+    *abort_flag = 0;
+    gb300::fence_mbar_init();
+  }
 
   const size_t head = (size_t)bh * N * kD;
   const float* qg = q + head;
@@ -105,52 +139,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *reinterpret_cast<float4*>(Qs + row * kQPad + c4 * 4) = val;
   }
+  __syncthreads();  // Q and the barriers are ready
 
   const int kv_limit = kCausal ? min(q0 + kBr, N) : N;
   const int Tc = (kv_limit + kBc - 1) / kBc;
 
-  float m_i[8], l_i[8], acc[8][4];
+  float m_i[kRows], l_i[kRows], acc[kRows][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < kRows; ++i) {
     m_i[i] = -INFINITY;
     l_i[i] = 0.f;
 #pragma unroll
     for (int d = 0; d < 4; ++d) acc[i][d] = 0.f;
   }
 
-  load_kv_block(kg, vg, Ks, Vs, 0, N, 0);
-  cp_async_commit();
+  // Each thread copies its share of every K/V block and reports completion
+  // on the block's full barrier; block j lives in buffer j % 3.
+  auto issue_load = [&](int jb) {
+    load_kv_block(kg, vg, Ks, Vs, jb * kBc, N, jb % kKvBufs);
+    cp_async_arrive(bar_full(jb % kKvBufs));
+  };
+  issue_load(0);
+  bool ok = true;
+  if (half == 1)
+    ok = gb300::mbar_wait(bar_go, 0, abort_flag, err, gb300::kSiteQFull, 0);
 
   for (int j = 0; j < Tc; ++j) {
-    const int buf = j & 1;
+    const int buf = j % kKvBufs;
     const int kv0 = j * kBc;
-    cp_async_wait_all();
-    __syncthreads();  // block j visible; everyone is done with block j-1
-    if (j + 1 < Tc) {
-      load_kv_block(kg, vg, Ks, Vs, kv0 + kBc, N, buf ^ 1);
-      cp_async_commit();
+    if (ok && j + 1 < Tc) {
+      // block j+1 goes where block j-2 was: every thread must be done with it
+      const int nb = (j + 1) % kKvBufs;
+      if (j + 1 >= kKvBufs)
+        ok = gb300::mbar_wait(bar_empty(nb), ((j + 1) / kKvBufs - 1) & 1, abort_flag, err,
+                              gb300::kSiteKvEmpty, j);
+      if (ok) issue_load(j + 1);
+    }
+    if (ok) ok = gb300::mbar_wait(bar_full(buf), (j / kKvBufs) & 1, abort_flag, err,
+                                  gb300::kSiteKvFull, j);
+    // One barrier of the half per block, after its waits (all bounded): the
+    // half leaves the loop together if any wait of the CTA has failed, and
+    // every thread of the half is done reading P of block j-1 (its PV).
+    if (gb300::named_barrier_any(1 + half, kThreads / 2, !ok || *abort_flag != 0)) {
+      ok = false;
+      break;
     }
 
     // ---- S = Q K^T for this thread's 8 x 4 tile (log2 units).  Packed
     // two-lane FMAs over pairs of d: each (row, key) keeps an even-d and an
     // odd-d partial sum, added once at the end.
-    float se[8][4], so[8][4];
+    float se[kRows][4], so[kRows][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) se[i][jj] = so[i][jj] = 0.f;
     const float* Kb = Ks + buf * kBc * kKPad;
 #pragma unroll 4
     for (int d4 = 0; d4 < kD / 4; ++d4) {
-      float4 qv[8], kv4[4];
+      float4 qv[kRows], kv4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        qv[i] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * i) * kQPad + d4 * 4);
+      for (int i = 0; i < kRows; ++i)
+        qv[i] = *reinterpret_cast<const float4*>(Qs + (ty + kTy * i) * kQPad + d4 * 4);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
         kv4[jj] = *reinterpret_cast<const float4*>(Kb + (tx + 16 * jj) * kKPad + d4 * 4);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < kRows; ++i)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           gb300::ffma2(se[i][jj], so[i][jj], qv[i].x, qv[i].y, kv4[jj].x, kv4[jj].y, se[i][jj],
@@ -159,9 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        so[i][jj]);
         }
     }
-    float s[8][4];
+    float s[kRows][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) s[i][jj] = se[i][jj] + so[i][jj];
 
@@ -170,18 +224,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool diag = kCausal && (kv0 + kBc - 1 > q0);
     if (tail || diag) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < kRows; ++i)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           int key = kv0 + tx + 16 * jj;
-          int row = q0 + ty + 16 * i;
+          int row = q0 + ty + kTy * i;
           if (key >= N || (kCausal && key > row)) s[i][jj] = -INFINITY;
         }
     }
 
     // ---- online softmax (base 2): m, rescale factors, P, l
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kRows; ++i) {
       float mt = fmaxf(fmaxf(s[i][0], s[i][1]), fmaxf(s[i][2], s[i][3]));
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1)
@@ -203,27 +257,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < 4; ++d) acc[i][d] *= alpha;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<float2*>(Ps + (ty + 16 * i) * kPPad + 2 * (tx + 16 * jj)) =
+        *reinterpret_cast<float2*>(Ps + (ty + kTy * i) * kPPad + 2 * (tx + 16 * jj)) =
             make_float2(s[i][jj], s[i][jj]);
     }
-    __syncthreads();  // P visible
+    gb300::named_barrier_sync(1 + half, kThreads / 2);  // the half's P rows are visible
+    if (j == 0 && half == 0) gb300::mbar_arrive(bar_go);
 
     // ---- O += P V for this thread's 8 x 4 tile: packed two-lane FMAs over
     // pairs of output columns, P read as (p, p) pairs
     const float* Vb = Vs + buf * kBc * kD;
 #pragma unroll 2
     for (int c4 = 0; c4 < kBc / 4; ++c4) {
-      float4 pa[8], pb[8], vv[4];
+      float4 pa[kRows], pb[kRows], vv[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * kPPad + c4 * 8);
-        pb[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * kPPad + c4 * 8 + 4);
+      for (int i = 0; i < kRows; ++i) {
+        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + kTy * i) * kPPad + c4 * 8);
+        pb[i] = *reinterpret_cast<const float4*>(Ps + (ty + kTy * i) * kPPad + c4 * 8 + 4);
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         vv[kk] = *reinterpret_cast<const float4*>(Vb + (c4 * 4 + kk) * kD + tx * 4);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kRows; ++i) {
         gb300::ffma2(acc[i][0], acc[i][1], pa[i].x, pa[i].y, vv[0].x, vv[0].y, acc[i][0], acc[i][1]);
         gb300::ffma2(acc[i][2], acc[i][3], pa[i].x, pa[i].y, vv[0].z, vv[0].w, acc[i][2], acc[i][3]);
         gb300::ffma2(acc[i][0], acc[i][1], pa[i].z, pa[i].w, vv[1].x, vv[1].y, acc[i][0], acc[i][1]);
@@ -234,13 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         gb300::ffma2(acc[i][2], acc[i][3], pb[i].z, pb[i].w, vv[3].z, vv[3].w, acc[i][2], acc[i][3]);
       }
     }
+    gb300::mbar_arrive(bar_empty(buf));  // this thread is done with block j's K and V
   }
+  // Half 0 may have stopped before letting half 1 start.
+  if (half == 0 && Tc == 0) gb300::mbar_arrive(bar_go);
+  cp_async_wait_all();  // every copy this thread started has landed
 
   // ---- epilogue: O = O / l (one division per row), LSE, single HBM write
+  if (!ok) return;
   constexpr float kLn2 = 0.69314718055994530942f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = q0 + ty + 16 * i;
+  for (int i = 0; i < kRows; ++i) {
+    const int row = q0 + ty + kTy * i;
     if (row >= N) continue;
     const float inv_l = 1.0f / l_i[i];
     float4 out = make_float4(acc[i][0] * inv_l, acc[i][1] * inv_l, acc[i][2] * inv_l,
@@ -276,13 +336,13 @@ cudaError_t launch_prefill_f32(const PrefillF32Args& a, cudaStream_t s) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     prefill_f32_kernel<true><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(
-        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale);
+        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale, a.err);
   } else {
     e = cudaFuncSetAttribute(prefill_f32_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     prefill_f32_kernel<false><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(
-        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale);
+        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale, a.err);
   }
   return cudaGetLastError();
 }
