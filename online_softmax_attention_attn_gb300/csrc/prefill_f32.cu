@@ -25,6 +25,9 @@
 // blocks sit in a ring of three buffers whose loads report on a full mbarrier
 // (cp.async.mbarrier.arrive) and whose reuse waits on an empty one.  Every
 // wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
+// Blocks are 128 query rows; a grid of fewer (head, block) pairs than half
+// the SMs runs with 32-row blocks instead (same 256 threads, two rows each),
+// so that a small problem spreads over four times as many SMs.
 #include <math.h>
 
 #include "common.cuh"
@@ -32,26 +35,25 @@
 namespace {
 
 constexpr int kD = 64;
-constexpr int kBr = 128;
+constexpr int kBrLarge = 128;          // query rows per CTA (a 32-row variant serves small grids)
+constexpr int kBrSmall = 32;
 constexpr int kBc = 64;
 constexpr int kThreads = 256;
 constexpr int kTy = 16;                 // row groups (rows interleaved by kTy)
-constexpr int kRows = kBr / kTy;        // query rows per thread
 constexpr int kKvBufs = 3;              // K/V blocks in shared memory
 constexpr int kQPad = kD + 4;  // 68 floats: 16-byte aligned rows, shifted banks
 constexpr int kKPad = kD + 4;
 constexpr int kPPad = 2 * kBc + 8;  // P stored as (p, p) pairs: 136 floats a row
-constexpr int kSmemFloats =
-    kBr * kQPad + kKvBufs * kBc * kKPad + kKvBufs * kBc * kD + kBr * kPPad;
-constexpr int kSmemBytes = kSmemFloats * 4 + (2 * kKvBufs + 1) * 8 + 16;  // + barriers, flag
+template <int kBr>
+constexpr int smem_bytes() {
+  return (kBr * kQPad + kKvBufs * kBc * kKPad + kKvBufs * kBc * kD + kBr * kPPad) * 4 +
+         (2 * kKvBufs + 1) * 8 + 16;  // + barriers, abort flag
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -83,11 +85,12 @@ __device__ __forceinline__ void load_kv_block(const float* __restrict__ kg,
   }
 }
 
-template <bool kCausal>
+template <int kBr, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                        const float* __restrict__ v, float* __restrict__ o,
                        float* __restrict__ lse, int BH, int N, float qscale, int* err) {
+  constexpr int kRows = kBr / kTy;  // query rows per thread
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
   float* Ks = Qs + kBr * kQPad;           // [3][Bc][68]
@@ -314,14 +317,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool prefill_f32_info(int D, int* Br, int* Bc, int* threads, int* smem) {
   if (D != kD) return false;
-  if (Br) *Br = kBr;
+  if (Br) *Br = kBrLarge;
   if (Bc) *Bc = kBc;
   if (threads) *threads = kThreads;
-  if (smem) *smem = kSmemBytes;
+  if (smem) *smem = smem_bytes<kBrLarge>();
   return true;
 }
 
-cudaError_t launch_prefill_f32(const PrefillF32Args& a, cudaStream_t s) {
+namespace {
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int kBr>
+cudaError_t launch_br(const PrefillF32Args& a, cudaStream_t s) {
   const int BH = a.B * a.H;
   const int n_qt = (a.N + kBr - 1) / kBr;
   const long long blocks = (long long)n_qt * BH;
@@ -330,19 +351,23 @@ cudaError_t launch_prefill_f32(const PrefillF32Args& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   const float qscale = a.scale * 1.4426950408889634f;  // log2(e)
-  cudaError_t e;
-  if (a.causal) {
-    e = cudaFuncSetAttribute(prefill_f32_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    prefill_f32_kernel<true><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(
-        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale, a.err);
-  } else {
-    e = cudaFuncSetAttribute(prefill_f32_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    prefill_f32_kernel<false><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(
-        a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale, a.err);
-  }
+  constexpr int kSmem = smem_bytes<kBr>();
+  auto kern = a.causal ? prefill_f32_kernel<kBr, true> : prefill_f32_kernel<kBr, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)blocks, kThreads, kSmem, s>>>(a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale,
+                                                  a.err);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// 128-row blocks, unless they would leave most of the GPU idle (fewer CTAs
+// than half its SMs): then 32-row blocks, four times as many CTAs each with
+// a quarter of the work per KV block.
+cudaError_t launch_prefill_f32(const PrefillF32Args& a, cudaStream_t s) {
+  const long long large = (long long)((a.N + kBrLarge - 1) / kBrLarge) * a.B * a.H;
+  const int nsm = sm_count();
+  if (nsm > 0 && 2 * large < nsm) return launch_br<kBrSmall>(a, s);
+  return launch_br<kBrLarge>(a, s);
 }

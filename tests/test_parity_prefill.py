@@ -83,6 +83,15 @@ def test_fp32_ragged(N, causal):
     _check_full(q, k, v, causal, 0.125)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [200, 321])
+def test_fp32_ragged_large_grid(N, causal):
+    """Enough (head, 128-row block) pairs to fill half the SMs, so the kernel
+    runs with 128-row blocks (the small cases above get 32-row blocks)."""
+    q, k, v = mha_inputs(4, 20, N, 64, torch.float32, seed=250 + N)
+    _check_full(q, k, v, causal, 0.125)
+
+
 def test_fp32_scale_zero_gives_prefix_means():
     q, k, v = mha_inputs(1, 2, 300, 64, torch.float32, seed=5)
     o, lse = _run(q, k, v, True, 0.0)
