@@ -282,7 +282,7 @@ ATTN_API int mla_decode_split(const void* q, const void* kv_cache,
  * Arguments and results are those of mla_decode minus the workspace; the
  * automatic split plan is used.  The plan and the split partials live in
  * one fixed array inside libattn.so (a file-scope static __device__ array of
- * 42,058,240 bytes, about 40.1 MiB), which every GPU that loads the library
+ * 21,218,048 bytes, about 20.2 MiB), which every GPU that loads the library
  * keeps until the process exits.
  *   Limits: B <= 8192 sequences and a device of at most 160 SMs; beyond
  *   them the call returns ATTN_ERR_UNSUPPORTED and launches nothing.

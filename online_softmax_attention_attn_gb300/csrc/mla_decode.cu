@@ -42,7 +42,8 @@
 //     chunk per cluster at a time (persistent).  The device planner either
 //     gives each sequence its own chunk (no partials) or cuts the flat order
 //     into equal chunks, moving cuts to nearby sequence starts; a sequence cut
-//     by a chunk edge writes fp32 partials that a small combine kernel merges.
+//     by a chunk edge writes partials (O / l as bf16 rows, the LSE in fp32)
+//     that a small combine kernel merges.
 //   * Every wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
 #include <math.h>
 
@@ -143,7 +144,7 @@ __host__ __device__ constexpr WsLayout ws_layout(int B, int max_chunks) {
   w.clist = align_up(w.cstart + sizeof(int) * (size_t)max_chunks, 16);
   w.plse = align_up(w.clist + sizeof(int4) * (size_t)B, 256);
   w.po = align_up(w.plse + sizeof(float) * (size_t)(2 * max_chunks) * kHq, 256);
-  w.total = align_up(w.po + sizeof(float) * (size_t)(2 * max_chunks) * kHq * kDv, 256);
+  w.total = align_up(w.po + sizeof(__nv_bfloat16) * (size_t)(2 * max_chunks) * kHq * kDv, 256);
   return w;
 }
 
@@ -274,19 +275,19 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const int32_t* __restric
     } else {
       pps = max(1, (T + clusters - 1) / max(clusters, 1));
       // time model: per-cluster pages (tensor-bound) vs bytes (HBM-bound),
-      // split partials cost 2 x 256 KB of traffic each
+      // split partials cost 2 x 128 KB of traffic each (bf16 rows)
       const float page_us = 0.65f, bytes_per_us = 6.5e6f;
       const float kv = (float)T * kPage * 1152.f;
       const int n_a = (T + pps - 1) / pps;
-      const float est_a = fmaxf(pps * page_us, (kv + 2.f * n_a * 2.f * 262144.f) / bytes_per_us);
+      const float est_a = fmaxf(pps * page_us, (kv + 2.f * n_a * 2.f * 131072.f) / bytes_per_us);
       const float est_b = fmaxf(maxn_s * page_us, kv / bytes_per_us);
       // fewer sequences than clusters: each sequence in ceil(n_b / L) chunks
       // of its own (no chunk spans two sequences), L the shortest chunk
       // length whose chunk count fits the clusters; each chunk of a cut
-      // sequence writes one partial (256 KB written, then read)
+      // sequence writes one partial (128 KB written, then read)
       const int len_c = len3_s, n_c = n3_s;
       const float est_c =
-          len_c > 0 ? fmaxf(len_c * page_us, (kv + 2.f * cut3_s * 262144.f) / bytes_per_us)
+          len_c > 0 ? fmaxf(len_c * page_us, (kv + 2.f * cut3_s * 131072.f) / bytes_per_us)
                     : 3.4e38f;
       if (B <= clusters && est_b <= est_a && est_b <= est_c) {
         mode = 1;
@@ -456,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       float* __restrict__ lse, const int* __restrict__ hdr,
                       const int* __restrict__ prefix, const int* __restrict__ bounds,
                       const int* __restrict__ cstart,
-                      float* __restrict__ part_lse, float* __restrict__ part_o, int B,
+                      float* __restrict__ part_lse, __nv_bfloat16* __restrict__ part_o, int B,
                       int max_blocks, int num_blocks, float scale_log2, int* err,
                       int debug_skip_step) {
   extern __shared__ uint8_t smem_raw[];
@@ -781,8 +782,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_st_wait();
     };
 
-    // O / l of this warp's rows and columns -> bf16 (whole sequence) or an
-    // fp32 partial; the LSE of its own heads.  The peer's heads take the row
+    // O / l of this warp's rows and columns -> bf16, into O (whole sequence)
+    // or into the segment's partial slot; the LSE of its own heads (fp32).  The peer's heads take the row
     // sums the peer sent.
     auto epilogue = [&]() -> bool {
       float lv = prev_l;
@@ -802,24 +803,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 128; c += 32) {
         float ov[32];
         tmem_ld32(tO + par * 128 + c, ov);
-        if (prev_slot < 0) {
-          __nv_bfloat16* dst = o + orow * kDv + col0 + c;
+        __nv_bfloat16* dst =
+            (prev_slot < 0 ? o + orow * kDv : part_o + ((size_t)prev_slot * kHq + h) * kDv) +
+            col0 + c;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
-            w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
-            w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
-            w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
-            *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
-          }
-        } else {
-          float* dst = part_o + ((size_t)prev_slot * kHq + h) * kDv + col0 + c;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<float4*>(dst + q4 * 4) =
-                make_float4(ov[q4 * 4] * inv_l, ov[q4 * 4 + 1] * inv_l, ov[q4 * 4 + 2] * inv_l,
-                            ov[q4 * 4 + 3] * inv_l);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
+          w.y = pack_bf16x2(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
+          w.z = pack_bf16x2(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
+          w.w = pack_bf16x2(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
+          *reinterpret_cast<uint4*>(dst + q4 * 8) = w;
         }
       }
       if (own && par == 0) {
@@ -1189,7 +1183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // loads deep.  With nothing listed every block exits at once.
 __global__ void __launch_bounds__(256) mla_combine_kernel(
     const int* __restrict__ hdr, const int* __restrict__ bounds, const int4* __restrict__ clist,
-    const float* __restrict__ part_lse, const float* __restrict__ part_o,
+    const float* __restrict__ part_lse, const __nv_bfloat16* __restrict__ part_o,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   grid_dependency_wait();  // the decode kernel's partials are complete
   const int rows = hdr[4] * kHq;
@@ -1223,7 +1217,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
         nz[u] = (k <= k1) ? bounds[k + 1] - bounds[k] : 0;
       }
       float ls[4];
-      float4 v[4][4];
+      uint4 v[4][2];  // 16 bf16 partial values a lane
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int k = kb + u;
@@ -1231,10 +1225,10 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
         ls[u] = -INFINITY;
         if (nz[u] > 0) {
           ls[u] = part_lse[(size_t)slot * kHq + h];
-          const float4* src =
-              reinterpret_cast<const float4*>(part_o + ((size_t)slot * kHq + h) * kDv + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v[u][q] = src[q];
+          const uint4* src =
+              reinterpret_cast<const uint4*>(part_o + ((size_t)slot * kHq + h) * kDv + c0);
+          v[u][0] = src[0];
+          v[u][1] = src[1];
         }
       }
 #pragma unroll
@@ -1244,12 +1238,12 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
         const float a = expf(mx - m_new);  // 0 while mx is still -inf
         const float w = expf(ls[u] - m_new);
         wsum = wsum * a + w;
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(v[u]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[4 * q] = acc[4 * q] * a + w * v[u][q].x;
-          acc[4 * q + 1] = acc[4 * q + 1] * a + w * v[u][q].y;
-          acc[4 * q + 2] = acc[4 * q + 2] * a + w * v[u][q].z;
-          acc[4 * q + 3] = acc[4 * q + 3] * a + w * v[u][q].w;
+        for (int q = 0; q < 8; ++q) {
+          const float2 f = unpack_bf16x2(pw[q]);
+          acc[2 * q] = acc[2 * q] * a + w * f.x;
+          acc[2 * q + 1] = acc[2 * q + 1] * a + w * f.y;
         }
         mx = m_new;
       }
@@ -1331,7 +1325,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   int* cstart = reinterpret_cast<int*>(ws + w.cstart);
   int4* clist = reinterpret_cast<int4*>(ws + w.clist);
   float* plse = reinterpret_cast<float*>(ws + w.plse);
-  float* po = reinterpret_cast<float*>(ws + w.po);
+  __nv_bfloat16* po = reinterpret_cast<__nv_bfloat16*>(ws + w.po);
 
   CUtensorMap mkv, mrope;
   CUresult r = make_map_2d(&mkv, a.kv, (long long)a.num_blocks * kPage, kStep, 64);
@@ -1381,7 +1375,7 @@ cudaError_t launch_mla_decode(const MlaArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, (const int*)hdr, (const int*)bounds,
-                         (const int4*)clist, (const float*)plse, (const float*)po,
+                         (const int4*)clist, (const float*)plse, (const __nv_bfloat16*)po,
                          static_cast<__nv_bfloat16*>(a.o), a.lse);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
