@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int qn[2] = {0, 0};     // Q loads per tile
       bool ok = true;
       int item = blockIdx.x;  // first item; later ones come from the launch's ticket
+      bool q0_issued = false; // this item's Q_0 went out during the previous item
       for (int k = 0; ok; ++k) {
         const int slot = k % kItemSlots;
         if (k >= kItemSlots) {
@@ -223,26 +224,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // done.  Q_0 goes first, then K/V block 0, then Q_1: tile 1 runs one
         // block longer than tile 0 at the end of a causal item, and block 0
         // need not wait for that.
-        auto load_q = [&](int t) -> bool {
-          if (it.T[t] == 0) return true;
+        auto load_q = [&](const Item& iq, int t) -> bool {
+          if (iq.T[t] == 0) return true;
           if (qn[t] > 0 &&
               !mbar_wait(bar_q_free(t), (qn[t] - 1) & 1, abort_flag, err, kSiteQFull, k))
             return false;
           mbar_arrive_expect_tx(bar_q_full(t), C::kTileBytes);
           for (int a = 0; a < C::kAtoms; ++a)
             tma_load_3d(sQ + t * C::kTileBytes + a * kAtomBytes, &tmQ, bar_q_full(t), a * 64,
-                        (2 * it.pr + t) * kBM, it.bh);
+                        (2 * iq.pr + t) * kBM, iq.bh);
           ++qn[t];
           return true;
         };
-        ok = load_q(0);
+        if (!q0_issued) ok = load_q(it, 0);
+        q0_issued = false;
         if (!ok) break;
         const int Tmax = max(it.T[0], it.T[1]);
-        // The next item is claimed two blocks before this item's last K/V
-        // load (about four blocks before the item ends), so that the
-        // claim's round trip to the counter is hidden behind those loads;
-        // items still go to the CTAs that free up first.
-        const int j_claim = max(0, Tmax - 2);
+        // The next item is claimed three blocks before this item's last K/V
+        // load, so that the claim's round trip to the counter is hidden
+        // behind those loads; items still go to the CTAs that free up first.
+        // When tile 1 runs a block longer (causal), the next item's Q_0 goes
+        // out right after tile 0's last K/V block: its buffer is free once
+        // tile 0's last S is done, which comes before tile 1's last block is
+        // loaded, so it is no longer late when the next item starts (issuing
+        // that item's first S ahead of tile 1's last PV, or an L2 prefetch of
+        // its Q tiles, measured slower).
+        const int j_claim = max(0, Tmax - 3);
+        const bool early_q0 = kCausal && it.T[1] == it.T[0] + 1;
         int next = total_items;
         for (int j = 0; j < Tmax; ++j, ++kv) {
           if (j == j_claim) next = (int)gridDim.x + atomicAdd(ticket, 1);
@@ -267,8 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                j * kBN, it.bh, pol_kv);
           }
           if (j == 0) {
-            ok = load_q(1);
+            ok = load_q(it, 1);
             if (!ok) break;
+          }
+          if (early_q0 && j == it.T[0] - 1 && next < total_items) {
+            ok = load_q(decode_item<kCausal>(next, BH, N), 0);
+            if (!ok) break;
+            q0_issued = true;
           }
         }
         item = next;
