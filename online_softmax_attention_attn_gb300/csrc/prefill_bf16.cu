@@ -279,6 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d_hint(dst + C::kTileBytes + a * kAtomBytes, &tmV, bar_kv_full(s), a * 64,
                                j * kBN, it.bh, pol_kv);
           }
+          // causal: block j+1 into L2 now, so that its load (issued once a
+          // stage frees) is served from L2 (one block ahead measured best of
+          // one to three; without a mask the prefetch costs more than it saves)
+          if (kCausal && j + 1 < Tmax)
+            for (int a = 0; a < C::kAtoms; ++a) {
+              tma_prefetch_3d(&tmK, a * 64, (j + 1) * kBN, it.bh);
+              tma_prefetch_3d(&tmV, a * 64, (j + 1) * kBN, it.bh);
+            }
           if (j == 0) {
             ok = load_q(it, 1);
             if (!ok) break;
