@@ -281,20 +281,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // causal: block j+1 into L2 now, so that its load (issued once a
           // stage frees) is served from L2 (one block ahead measured best of
-          // one to three; without a mask the prefetch costs more than it saves)
-          if (kCausal && j + 1 < Tmax)
-            for (int a = 0; a < C::kAtoms; ++a) {
-              tma_prefetch_3d(&tmK, a * 64, (j + 1) * kBN, it.bh);
-              tma_prefetch_3d(&tmV, a * 64, (j + 1) * kBN, it.bh);
-            }
+          // one to three; without a mask the prefetch costs more than it
+          // saves).  Where the next item's Q_0 goes out at this block, the
+          // prefetch follows it, so that the Q tile, whose arrival sets the
+          // item boundary, does not queue behind it.
+          auto prefetch_next_block = [&]() {
+            if (kCausal && j + 1 < Tmax)
+              for (int a = 0; a < C::kAtoms; ++a) {
+                tma_prefetch_3d(&tmK, a * 64, (j + 1) * kBN, it.bh);
+                tma_prefetch_3d(&tmV, a * 64, (j + 1) * kBN, it.bh);
+              }
+          };
+          const bool q0_here = early_q0 && j == it.T[0] - 1 && next < total_items;
+          if (!q0_here) prefetch_next_block();
           if (j == 0) {
             ok = load_q(it, 1);
             if (!ok) break;
           }
-          if (early_q0 && j == it.T[0] - 1 && next < total_items) {
+          if (q0_here) {
             ok = load_q(decode_item<kCausal>(next, BH, N), 0);
             if (!ok) break;
             q0_issued = true;
+            prefetch_next_block();
           }
         }
         item = next;
