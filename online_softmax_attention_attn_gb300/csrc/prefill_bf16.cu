@@ -17,11 +17,13 @@
 //   * warp 8  : TMA producer and work source.  Per item: each Q tile as soon
 //               as the previous item's last S MMA of that tile is done, then
 //               K_j and V_j together into a ring of stages (128-byte
-//               swizzle), one full and one empty mbarrier per stage.  The next
-//               item is claimed from the launch's ticket counter a few blocks
-//               before this one ends, so items go to the CTAs that free up
-//               first; its number reaches the other warps through a 4-slot
-//               ring in shared memory.
+//               swizzle), one full and one empty mbarrier per stage; with the
+//               causal mask also K/V block j+1 into L2 right after block j's
+//               load.  The next item is claimed from the launch's ticket
+//               counter three blocks before this one's last load, so items
+//               go to the CTAs that free up first (in a causal item its Q_0
+//               goes out right after tile 0's last block); its number reaches
+//               the other warps through a 4-slot ring in shared memory.
 //   * warp 9  : MMA issuer (one thread) and TMEM owner.  For tile t,
 //               S_t = Q_t K_j^T (tcgen05.mma M=128 N=128 K=D) into TMEM, and
 //               O_t += P_t V_j with P read straight from TMEM as the A operand,
