@@ -370,6 +370,24 @@ ATTN_API int attn_fwd_test_skip_load(const void* q, const void* k, const void* v
                             int skip_load_index);
 
 /*
+ * attn_fwd_f32_test_skip_load -- TEST HOOK for the bounded-wait failure path
+ * of the fp32 CUDA-core kernel.
+ *
+ * Same as attn_fwd with dtype = ATTN_DTYPE_F32 (D = 64), except that no thread
+ * of any CTA copies K/V block `skip_block` (>= 0, 64 keys each) or reports it
+ * on the block's full mbarrier.  The CTA's bounded waits on that block (and,
+ * for block 0, the second half's wait for the first half to start it) run out
+ * after about 2 s, the kernel records ATTN_ERR_DEVICE_TIMEOUT, each thread
+ * lets its own copies land and returns, and attn_device_status() returns the
+ * code.  Nothing hangs, faults or traps.  Output contents are unspecified.
+ * Not for production use.
+ */
+ATTN_API int attn_fwd_f32_test_skip_load(const float* q, const float* k, const float* v,
+                                         float* o, float* lse, int B, int H, int N, int D,
+                                         int causal, float scale, void* stream,
+                                         int skip_block);
+
+/*
  * attn_fwd_tf32x3_test_skip_load -- TEST HOOK for the bounded-wait failure
  * path of attn_fwd_tf32x3.
  *

@@ -36,6 +36,7 @@ __all__ = [
     "mla_decode_workspace_size", "mla_decode_split_workspace_size", "mla_decode_noalloc", "mla_absorb_q", "mla_project_out",
     "attn_device_status", "attn_last_error",
     "attn_kv_tiles", "attn_kernel_info", "attn_fwd_test_skip_load",
+    "attn_fwd_f32_test_skip_load",
     "attn_fwd_tf32x3_test_skip_load", "mla_decode_test_skip_load",
     "LIB_PATH", "ATTN_DTYPE_F32", "ATTN_DTYPE_BF16",
 ]
@@ -82,6 +83,9 @@ def lib():
         L.attn_fwd_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                               _f, _vp, _i]
         L.attn_fwd_test_skip_load.restype = _i
+        L.attn_fwd_f32_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                                  _f, _vp, _i]
+        L.attn_fwd_f32_test_skip_load.restype = _i
         L.attn_fwd_tf32x3_test_skip_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i,
                                                      _i, _i, _f, _vp, _sz, _vp, _i]
         L.attn_fwd_tf32x3_test_skip_load.restype = _i
@@ -325,6 +329,15 @@ def attn_fwd_test_skip_load(q, k, v, o, lse, causal: bool, scale: float, skip_lo
     _check(lib().attn_fwd_test_skip_load(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                          N, D, int(bool(causal)), float(scale),
                                          _stream_ptr(stream), int(skip_load_index)))
+
+
+def attn_fwd_f32_test_skip_load(q, k, v, o, lse, causal: bool, scale: float, skip_block: int,
+                                stream=None):
+    """Test hook: fp32 attn_fwd (CUDA cores) in which no CTA loads one K/V block."""
+    B, H, N, D = q.shape
+    _check(lib().attn_fwd_f32_test_skip_load(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B,
+                                             H, N, D, int(bool(causal)), float(scale),
+                                             _stream_ptr(stream), int(skip_block)))
 
 
 def attn_fwd_tf32x3_test_skip_load(q, k, v, o, lse, causal: bool, scale: float,

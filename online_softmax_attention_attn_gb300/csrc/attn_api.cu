@@ -133,9 +133,10 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
   if (!err) return code;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == ATTN_DTYPE_F32) {
+    // the fp32 hook passes its K/V block index plus one (0: none)
     PrefillF32Args a{static_cast<const float*>(q), static_cast<const float*>(k),
                      static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, N, D,
-                     causal != 0, scale, err};
+                     causal != 0, scale, err, debug_skip_load - 1};
     return finish_launch(launch_prefill_f32(a, s), "attn_fwd");
   }
   int nsm = sm_count(&code);
@@ -149,6 +150,16 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
                         int B, int H, int N, int D, int causal, float scale, int dtype,
                         void* stream) {
   return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, dtype, stream, 0);
+}
+
+extern "C" int attn_fwd_f32_test_skip_load(const float* q, const float* k, const float* v,
+                                           float* o, float* lse, int B, int H, int N, int D,
+                                           int causal, float scale, void* stream,
+                                           int skip_block) {
+  if (skip_block < 0)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_f32_test_skip_load: block must be >= 0");
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, D, causal, scale, ATTN_DTYPE_F32, stream,
+                       skip_block + 1);
 }
 
 extern "C" int attn_fwd_test_skip_load(const void* q, const void* k, const void* v, void* o,

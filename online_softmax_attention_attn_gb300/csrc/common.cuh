@@ -80,6 +80,7 @@ struct PrefillF32Args {
   int causal;
   float scale;
   int* err;
+  int debug_skip_block;  // test hook: >=0 makes every CTA skip that K/V block's load
 };
 
 struct PrefillBf16Args {

@@ -89,7 +89,8 @@ template <int kBr, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                        const float* __restrict__ v, float* __restrict__ o,
-                       float* __restrict__ lse, int BH, int N, float qscale, int* err) {
+                       float* __restrict__ lse, int BH, int N, float qscale, int* err,
+                       int debug_skip_block) {
   constexpr int kRows = kBr / kTy;  // query rows per thread
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each thread copies its share of every K/V block and reports completion
   // on the block's full barrier; block j lives in buffer j % 3.
   auto issue_load = [&](int jb) {
+    if (jb == debug_skip_block) return;  // test hook: this block never arrives
     load_kv_block(kg, vg, Ks, Vs, jb * kBc, N, jb % kKvBufs);
     cp_async_arrive(bar_full(jb % kKvBufs));
   };
@@ -356,7 +358,7 @@ cudaError_t launch_br(const PrefillF32Args& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)blocks, kThreads, kSmem, s>>>(a.q, a.k, a.v, a.o, a.lse, BH, a.N, qscale,
-                                                  a.err);
+                                                  a.err, a.debug_skip_block);
   return cudaGetLastError();
 }
 

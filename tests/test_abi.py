@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
     for n in ["attn_fwd", "mla_decode", "mla_decode_split", "mla_decode_workspace_size",
               "mla_decode_split_workspace_size",
               "attn_device_status", "attn_last_error", "attn_kv_tiles", "attn_kernel_info",
-              "attn_fwd_test_skip_load", "mla_absorb_q", "mla_project_out",
+              "attn_fwd_test_skip_load", "attn_fwd_f32_test_skip_load", "mla_absorb_q",
+              "mla_project_out",
               "attn_fwd_tf32x3", "attn_fwd_tf32x3_workspace_size", "attn_fwd_host",
               "attn_fwd_host_workspace_size", "mla_decode_host",
               "mla_decode_host_workspace_size"]:

@@ -79,6 +79,41 @@ def test_stuck_tf32x3_pipeline_reports_timeout_and_context_survives():
     assert np.abs(lse2.cpu().numpy() - rl).max() <= 1e-4
 
 
+@pytest.mark.parametrize("skip_block,N,B,H", [(0, 256, 1, 2), (2, 512, 1, 20)])
+def test_stuck_f32_pipeline_reports_timeout_and_context_survives(skip_block, N, B, H):
+    """fp32 attn_fwd (CUDA cores) with one K/V block never loaded, with the
+    32-row and the 128-row blocks: every CTA's bounded wait on that block runs
+    out (for block 0 also the second half's wait for the first half to start),
+    the CTAs unwind, and the next call is correct."""
+    dev = torch.device("cuda")
+    q, k, v = mha_inputs(B, H, N, 64, torch.float32, seed=83 + skip_block)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(dq)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    t0 = time.time()
+    pkg.attn_fwd_f32_test_skip_load(dq, dk, dv, o, lse, False, 0.125, skip_block)
+    code = pkg.attn_device_status(raise_on_error=False)
+    elapsed = time.time() - t0
+    assert code == pkg.ATTN_ERR_DEVICE_TIMEOUT, pkg.attn_last_error()
+    assert "wait ran out" in pkg.attn_last_error()
+    assert elapsed < 30
+    assert pkg.attn_device_status(raise_on_error=False) == pkg.ATTN_OK
+    o2, lse2 = pkg.attn_fwd(dq, dk, dv, causal=False, scale=0.125)
+    pkg.attn_device_status()
+    ro, rl = oracle.mha(q, k, v, False, 0.125)
+    assert np.abs(o2.cpu().numpy() - ro).max() <= 1e-4
+    assert np.abs(lse2.cpu().numpy() - rl).max() <= 1e-4
+
+
+def test_f32_skip_hook_rejects_bad_index():
+    dev = torch.device("cuda")
+    z = torch.zeros(1, 1, 128, 64, dtype=torch.float32, device=dev)
+    with pytest.raises(pkg.AttnError):
+        pkg.attn_fwd_f32_test_skip_load(z, z, z, z.clone(), torch.empty(1, 1, 128, device=dev),
+                                        False, 0.1, -1)
+
+
 def test_stuck_decode_cluster_reports_timeout_and_context_survives():
     """mla_decode in which rank 1 of every cluster never loads its fourth
     step: rank 1 times out waiting for the page, rank 0 times out waiting for
