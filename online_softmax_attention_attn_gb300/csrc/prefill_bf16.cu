@@ -20,7 +20,7 @@
 //               swizzle), one full and one empty mbarrier per stage; with the
 //               causal mask also K/V block j+1 into L2 right after block j's
 //               load.  The next item is claimed from the launch's ticket
-//               counter three blocks before this one's last load, so items
+//               counter five blocks before this one's last load, so items
 //               go to the CTAs that free up first (in a causal item its Q_0
 //               goes out right after tile 0's last block); its number reaches
 //               the other warps through a 4-slot ring in shared memory.
@@ -247,16 +247,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         q0_issued = false;
         if (!ok) break;
         const int Tmax = max(it.T[0], it.T[1]);
-        // The next item is claimed three blocks before this item's last K/V
-        // load, so that the claim's round trip to the counter is hidden
-        // behind those loads; items still go to the CTAs that free up first.
+        // The next item is claimed five blocks before this item's last K/V
+        // load, so that the claim's round trip to the counter (1-2.5 us) is
+        // hidden behind those loads (three, five, six and eight measured;
+        // five on); items still go to the CTAs that free up first.
         // When tile 1 runs a block longer (causal), the next item's Q_0 goes
         // out right after tile 0's last K/V block: its buffer is free once
         // tile 0's last S is done, which comes before tile 1's last block is
         // loaded, so it is no longer late when the next item starts (issuing
         // that item's first S ahead of tile 1's last PV, or an L2 prefetch of
         // its Q tiles, measured slower).
-        const int j_claim = max(0, Tmax - 3);
+        const int j_claim = max(0, Tmax - 5);
         const bool early_q0 = kCausal && it.T[1] == it.T[0] + 1;
         int next = total_items;
         for (int j = 0; j < Tmax; ++j, ++kv) {
