@@ -14,7 +14,8 @@ The default run also reports
   * `configs`: every other workload of the target list (the fp32 small causal
     case and the fp32 B4 H8 N8192 D64 case, both masks, on the CUDA cores and
     on the tensor cores; the non-causal bf16 prefill; the paged batch-256
-    decode; the decode batch sweep), each with its median time, throughput,
+    decode; the decode batch sweep), each with its median time (at least 50
+    L2-flushed calls after 10 warm-up calls), throughput,
     fractions of the measured and spec peaks, and its output checked against
     the fp64 oracle (every row, or a seeded sample of rows for the largest);
   * `cpu_baseline`: the oracle's own time on every row of the step's prefill,
