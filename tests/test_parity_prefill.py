@@ -179,6 +179,16 @@ def test_bf16_many_items_per_cta(causal):
     _check_sampled(q, k, v, causal, 1.0 / math.sqrt(D), o, lse, nrows=768, seed=7)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_item_boundaries_every_row(causal):
+    """200 heads (full head groups plus a short last one) x 2 Q-tile pairs
+    with a ragged last tile (N = 500): 400 work items, two or three per
+    persistent CTA, so the next item's Q_0 load, the early claim and the L2
+    prefetch of K/V all cross item boundaries; every output row is checked."""
+    q, k, v = mha_inputs(2, 100, 500, 128, torch.bfloat16, seed=61 + int(causal))
+    _check_full(q, k, v, causal, 1.0 / math.sqrt(128))
+
+
 def test_bf16_more_launches_than_ticket_slots():
     """Each launch draws its items from one of a fixed set of counters; many
     launches in a row reuse them and every result stays the same."""
