@@ -17,9 +17,11 @@
 // 68-float rows bank-conflict free for 128-bit loads.  Both products use the
 // packed two-lane FMA (fma.rn.f32x2), half the instructions of scalar FFMAs:
 // S over pairs of d (even and odd partial sums per element, added at the
-// end), PV over pairs of output columns with P kept in shared memory as
-// (p, p) pairs.  Softmax runs in base 2 with log2(e) folded into the Q
-// pre-scale.  The CTA's two halves (warps 0-3 and 4-7, 64 interleaved rows
+// end), PV over pairs of output columns, each P value (stored once in shared
+// memory) multiplying both lanes.  Shared-memory loads, not the FMA pipe, set
+// the pace of these loops, so P is not stored twice as a (p, p) pair and
+// both loops are unrolled eight steps deep.  Softmax runs in base 2 with
+// log2(e) folded into the Q pre-scale.  The CTA's two halves (warps 0-3 and 4-7, 64 interleaved rows
 // each) synchronise only among themselves and run the KV loop half a block
 // apart, so that one half's softmax overlaps the other half's FMA loops: K/V
 // blocks sit in a ring of three buffers whose loads report on a full mbarrier
@@ -43,7 +45,7 @@ constexpr int kTy = 16;                 // row groups (rows interleaved by kTy)
 constexpr int kKvBufs = 3;              // K/V blocks in shared memory
 constexpr int kQPad = kD + 4;  // 68 floats: 16-byte aligned rows, shifted banks
 constexpr int kKPad = kD + 4;
-constexpr int kPPad = 2 * kBc + 8;  // P stored as (p, p) pairs: 136 floats a row
+constexpr int kPPad = kBc + 16;  // P: 80 floats a row (the two rows of a warp 16 banks apart)
 template <int kBr>
 constexpr int smem_bytes() {
   return (kBr * kQPad + kKvBufs * kBc * kKPad + kKvBufs * kBc * kD + kBr * kPPad) * 4 +
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
   float* Ks = Qs + kBr * kQPad;           // [3][Bc][68]
   float* Vs = Ks + kKvBufs * kBc * kKPad; // [3][Bc][64]
-  float* Ps = Vs + kKvBufs * kBc * kD;    // [Br][136]: each P twice, (p, p)
+  float* Ps = Vs + kKvBufs * kBc * kD;    // [Br][80]: P of the current block
   uint64_t* bars = reinterpret_cast<uint64_t*>(Ps + kBr * kPPad);  // full[3], empty[3], go
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kKvBufs + 1);
   const uint32_t bar0 = gb300::smem_u32(bars);
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) se[i][jj] = so[i][jj] = 0.f;
     const float* Kb = Ks + buf * kBc * kKPad;
-#pragma unroll 4
+#pragma unroll 8
     for (int d4 = 0; d4 < kD / 4; ++d4) {
       float4 qv[kRows], kv4[4];
 #pragma unroll
@@ -262,36 +264,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < 4; ++d) acc[i][d] *= alpha;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<float2*>(Ps + (ty + kTy * i) * kPPad + 2 * (tx + 16 * jj)) =
-            make_float2(s[i][jj], s[i][jj]);
+        Ps[(ty + kTy * i) * kPPad + tx + 16 * jj] = s[i][jj];
     }
     gb300::named_barrier_sync(1 + half, kThreads / 2);  // the half's P rows are visible
     if (j == 0 && half == 0) gb300::mbar_arrive(bar_go);
 
     // ---- O += P V for this thread's 8 x 4 tile: packed two-lane FMAs over
-    // pairs of output columns, P read as (p, p) pairs
+    // pairs of output columns, one P value for both lanes
     const float* Vb = Vs + buf * kBc * kD;
-#pragma unroll 2
+#pragma unroll 8
     for (int c4 = 0; c4 < kBc / 4; ++c4) {
-      float4 pa[kRows], pb[kRows], vv[4];
+      float4 pa[kRows], vv[4];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + kTy * i) * kPPad + c4 * 8);
-        pb[i] = *reinterpret_cast<const float4*>(Ps + (ty + kTy * i) * kPPad + c4 * 8 + 4);
-      }
+      for (int i = 0; i < kRows; ++i)
+        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + kTy * i) * kPPad + c4 * 4);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         vv[kk] = *reinterpret_cast<const float4*>(Vb + (c4 * 4 + kk) * kD + tx * 4);
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
-        gb300::ffma2(acc[i][0], acc[i][1], pa[i].x, pa[i].y, vv[0].x, vv[0].y, acc[i][0], acc[i][1]);
-        gb300::ffma2(acc[i][2], acc[i][3], pa[i].x, pa[i].y, vv[0].z, vv[0].w, acc[i][2], acc[i][3]);
-        gb300::ffma2(acc[i][0], acc[i][1], pa[i].z, pa[i].w, vv[1].x, vv[1].y, acc[i][0], acc[i][1]);
-        gb300::ffma2(acc[i][2], acc[i][3], pa[i].z, pa[i].w, vv[1].z, vv[1].w, acc[i][2], acc[i][3]);
-        gb300::ffma2(acc[i][0], acc[i][1], pb[i].x, pb[i].y, vv[2].x, vv[2].y, acc[i][0], acc[i][1]);
-        gb300::ffma2(acc[i][2], acc[i][3], pb[i].x, pb[i].y, vv[2].z, vv[2].w, acc[i][2], acc[i][3]);
-        gb300::ffma2(acc[i][0], acc[i][1], pb[i].z, pb[i].w, vv[3].x, vv[3].y, acc[i][0], acc[i][1]);
-        gb300::ffma2(acc[i][2], acc[i][3], pb[i].z, pb[i].w, vv[3].z, vv[3].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].x, pa[i].x, vv[0].x, vv[0].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].x, pa[i].x, vv[0].z, vv[0].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].y, pa[i].y, vv[1].x, vv[1].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].y, pa[i].y, vv[1].z, vv[1].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].z, pa[i].z, vv[2].x, vv[2].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].z, pa[i].z, vv[2].z, vv[2].w, acc[i][2], acc[i][3]);
+        gb300::ffma2(acc[i][0], acc[i][1], pa[i].w, pa[i].w, vv[3].x, vv[3].y, acc[i][0], acc[i][1]);
+        gb300::ffma2(acc[i][2], acc[i][3], pa[i].w, pa[i].w, vv[3].z, vv[3].w, acc[i][2], acc[i][3]);
       }
     }
     gb300::mbar_arrive(bar_empty(buf));  // this thread is done with block j's K and V
