@@ -877,6 +877,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_q_full);
         }
+        // the next segment of this chunk: this thread's q lines into L2, so
+        // that its load at the segment change does not wait on DRAM
+        if (it.start < it.end && it.b < B) {
+          const char* nq = reinterpret_cast<const char*>(q + ((size_t)it.b * kHq + h) * kDk);
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + atom_col(2 * par) * 2));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + atom_col(2 * par) * 2 + 128));
+          if (par == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + rope_col * 2));
+        }
         // ---- the previous segment's epilogue overlaps this segment's first S
         if (prev_b >= 0) {
           ok = __all_sync(0xffffffffu,
